@@ -1,0 +1,563 @@
+#!/usr/bin/env python3
+"""Benchmark: decode-attention microseconds per layer-step and HBM GB/s vs roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--mode prop|flash|exact] [--workload NAME] [--S S]
+
+One step is one decode-attention layer-step of the workload (all kernels of one
+C-ABI call) over seeded synthetic inputs already resident in HBM.  Steps are
+replayed from CUDA graphs of --graph-steps consecutive calls; successive calls
+rotate through copies of the K/V cache whose total size exceeds 4x the L2 cache,
+so no call finds its cache in L2.  Timing uses CUDA events on the launching
+stream with a barrier and a synchronize on both sides; with N GPUs (torchrun,
+one process per GPU) every rank runs its own replica of the workload and the
+time is the maximum over ranks.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle on the host cores instead (each step one
+query head of the same layer-step; the value is scaled to a whole layer-step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/layer-step and HBM GB/s vs roofline, n_k=32k, S=128"
+UNIT = "us/layer-step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- setup
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=15000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["prop", "flash", "exact"], default="prop")
+    ap.add_argument("--workload", default="llama8b_32k_b1")
+    ap.add_argument("--S", type=int, default=0, help="override the workload's sample count")
+    ap.add_argument("--graph-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
+    ap.add_argument("--no-extras", action="store_true", help="skip the exact/flash comparison timings")
+    return ap.parse_args(argv)
+
+
+class Dist:
+    """Rank bookkeeping; a process group only when launched by torchrun with N > 1."""
+
+    def __init__(self, backend: str | None = None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            if backend is None:
+                import torch
+
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            if self.pg.get_backend() == "nccl":
+                import torch
+
+                self.pg.barrier(device_ids=[torch.cuda.current_device()])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        """Maximum of a float over ranks."""
+        if self.pg is None:
+            return float(x)
+        import torch
+
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate_value(max_elapsed_ms: float, steps: int, world: int) -> float:
+    """Whole-job microseconds per layer-step: every rank ran `steps` layer-steps of
+    its own replica within max_elapsed_ms, so the job did world * steps of them."""
+    return max_elapsed_ms * 1000.0 / (steps * world)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "stochastic_sparse_decode_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources (the summary records their digest)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_digest") != source_digest():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu, self.period, self.proc, self.path = gpu_index, period_ms, None, None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period}"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- byte model
+
+
+def byte_model(inp, mode: str, S: int, sample_idx=None):
+    """Algorithmic HBM bytes of one call and of its dominant kernel.
+
+    prop:  K (Hkv * sum L * d * e) + q + stash write (Hq * sum L * 4) + tile
+           records (written by pass 1, read by pass 2: 2 * 8 * B * Hq * T) +
+           stash read of the tiles that received samples (4 * len per tile) +
+           the distinct V rows the samples touch (d * e each, per KV head) + out.
+    flash: K + q + distinct V rows + tile partials and records (written and read) + out.
+    exact: K + V + q + tile partials and records (written and read) + out.
+    Pass 1 / the tile kernel: K + q + its writes.
+    """
+    w = inp.workload
+    e = 2 if w.dtype == "bf16" else 4
+    L = inp.lengths.astype(np.int64)
+    T = -(-L // w.tile)
+    sumL, sumT = int(L.sum()), int(T.sum())
+    B, Hq, Hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+    K = Hkv * sumL * d * e
+    q = B * Hq * d * e
+    out = B * Hq * d * 4
+    rec = 8 * Hq * sumT  # (m_t, z_t) per (b, h, t)
+    vrows = 0
+    stash_read = 0
+    if sample_idx is not None and mode in ("prop", "flash"):
+        G = w.group
+        for b in range(B):
+            for g in range(Hkv):
+                heads = sample_idx[b, g * G : (g + 1) * G]
+                rows = np.unique(heads[heads >= 0])
+                vrows += rows.size
+                if mode == "prop":
+                    for h in range(G):
+                        ts = np.unique(sample_idx[b, g * G + h] // w.tile)
+                        for t in ts:
+                            stash_read += 4 * int(min(w.tile, L[b] - t * w.tile))
+    if mode == "prop":
+        main = K + q + Hq * sumL * 4 + rec
+        total = main + rec + stash_read + vrows * d * e + out
+    elif mode == "flash":
+        part = 4 * Hq * sumT * d
+        main = K + q + rec + part + vrows * d * e
+        total = main + rec + part + out
+    else:
+        part = 4 * Hq * sumT * d
+        main = 2 * K + q + rec + part
+        total = main + rec + part + out
+    return {"total": int(total), "main": int(main), "v_rows": int(vrows), "stash_read": int(stash_read),
+            "k_bytes": int(K)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def run_ours(args, dist: Dist):
+    import torch
+
+    import stochastic_sparse_decode_gb300 as sd
+    from stochastic_sparse_decode_gb300.build import build
+    from stochastic_sparse_decode_gb300.decoder import Decoder
+    from synthetic import generate, get_workload, max_length, to_torch
+
+    build()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    w = get_workload(args.workload)
+    if args.S:
+        w = w.with_(S=args.S)
+    elif args.mode == "flash" and args.workload.startswith("llama8b"):
+        w = w.with_(S=2048)  # the flash mode's configuration (6.25% of n_k)
+    inp = generate(w)
+    q, k, v, indptr, U = to_torch(inp, dev)
+    dec = Decoder(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, inp.total_tokens, max_length(w), w.tile,
+                  w.S, w.dtype, device=dev)
+    out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+
+    # one debug call: sample indices for the byte model
+    dbg, bufs = dec.debug_buffers(args.mode, sample_stride=max(1, -(-w.S // max(1, int((-(-inp.lengths // w.tile)).min())))))
+    dec(args.mode, q, k, v, indptr, U, out=out, debug=dbg)
+    torch.cuda.synchronize()
+    sidx = bufs.get("sample_idx")
+    sidx = sidx.cpu().numpy().reshape(w.batch, w.num_q_heads, -1) if sidx is not None else None
+    bm = byte_model(inp, args.mode, w.S, sidx)
+
+    # L2-safe rotation of the K/V cache
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = k.numel() * k.element_size() + v.numel() * v.element_size()
+    nrot = max(2, math.ceil(4 * l2 / per_copy) + 1)
+    ks, vs = [k], [v]
+    for _ in range(nrot - 1):
+        ks.append(k.clone())
+        vs.append(v.clone())
+    for i in range(nrot):  # warm every descriptor / attribute before capture
+        dec(args.mode, q, ks[i], vs[i], indptr, U, out=out)
+    torch.cuda.synchronize()
+
+    def capture(nsteps, mode=args.mode, decoder=dec, Uarg=U):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(min(nsteps, nrot)):
+                decoder(mode, q, ks[i % nrot], vs[i % nrot], indptr, Uarg, out=out)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(nsteps):
+                decoder(mode, q, ks[i % nrot], vs[i % nrot], indptr, Uarg, out=out)
+        return g
+
+    def timed(nsteps, warm, mode=args.mode, decoder=dec, Uarg=U, sampler=None):
+        R = max(1, min(args.graph_steps, nsteps))
+        full, rem = divmod(nsteps, R)
+        g = capture(R, mode, decoder, Uarg)
+        gr = capture(rem, mode, decoder, Uarg) if rem else None
+        wf, wr = divmod(warm, R)
+        for _ in range(wf):
+            g.replay()
+        if wr:
+            capture(wr, mode, decoder, Uarg).replay()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+        dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(full):
+            g.replay()
+        if gr is not None:
+            gr.replay()
+        b.record()
+        b.synchronize()
+        torch.cuda.synchronize()
+        dist.barrier()
+        clocks = sampler.stop() if sampler else None
+        return a.elapsed_time(b), clocks
+
+    sampler = ClockSampler(dist.local_rank)
+    elapsed_ms, clocks = timed(args.steps, args.warmup, sampler=sampler)
+    max_ms = dist.max(elapsed_ms)
+    value = aggregate_value(max_ms, args.steps, dist.world)
+    per_step_us = elapsed_ms * 1000.0 / args.steps
+
+    # dominant kernel alone: events around it inside each call, GPU kept ahead of the host
+    nmain = 200
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nmain)]
+    dbgs = []
+    for a_, b_ in evs:
+        a_.record()  # torch creates the CUDA event on its first record
+        b_.record()
+        d_ = sd.Debug()
+        d_.main_begin = a_.cuda_event
+        d_.main_end = b_.cuda_event
+        dbgs.append(d_)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(50e6))  # ~25 ms of spinning so all launches below queue up
+    for i in range(nmain):
+        dec(args.mode, q, ks[i % nrot], vs[i % nrot], indptr, U, out=out, debug=dbgs[i])
+    torch.cuda.synchronize()
+    main_us = statistics.mean(a_.elapsed_time(b_) * 1000.0 for a_, b_ in evs[10:])
+    peak, peak_kind = measured_peaks()
+    kernel_name = {"prop": "prop_pass1", "flash": "flash_tile", "exact": "exact_tile"}[args.mode]
+    achieved = bm["main"] / (main_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(kernel_name, w.name),
+                "kernel": kernel_name, "kernel_us": round(main_us, 3), "algorithmic_bytes": bm["main"],
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
+                f"{peak_kind} (no MEASURED_PEAKS.json)"}
+
+    # end to end through the public API with pinned host buffers
+    hq_, hk, hv, hind, hU = (t.cpu().pin_memory() for t in (q, k, v, indptr, U))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv, dind, dU = (torch.empty_like(t, device=dev) for t in (q, k, v, indptr, U))
+    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk, hv, hind, hU))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for dst, src in ((dq, hq_), (dk, hk), (dv, hv), (dind, hind), (dU, hU)):
+            dst.copy_(src, non_blocking=True)
+        dec(args.mode, dq, dk, dv, dind, dU, out=out)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    b.record()
+    b.synchronize()
+    e2e_ms = dist.max(a.elapsed_time(b))
+    e2e = {"value": round(aggregate_value(e2e_ms, args.e2e_steps, dist.world), 3), "unit": UNIT,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+    del dq, dk, dv, hk, hv
+
+    extras = {}
+    if not args.no_extras and args.mode == "prop":
+        n_x = min(args.steps, 5000)
+        ms, _ = timed(n_x, min(args.warmup, 200), mode="exact")
+        exact_us = ms * 1000.0 / n_x
+        extras["exact_us_per_layer_step"] = round(exact_us, 3)
+        extras["speedup_vs_exact"] = round(exact_us / per_step_us, 3)
+        if w.name.startswith("llama8b"):
+            wf = w.with_(S=2048)
+            from synthetic.workloads import draw_offsets
+
+            Uf = torch.from_numpy(draw_offsets(2048, (w.batch, w.num_q_heads), np.random.default_rng(7))).to(dev)
+            decf = Decoder(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, inp.total_tokens, max_length(w),
+                           w.tile, 2048, w.dtype, device=dev)
+            for i in range(nrot):
+                decf("flash", q, ks[i], vs[i], indptr, Uf, out=out)
+            ms, _ = timed(n_x, min(args.warmup, 200), mode="flash", decoder=decf, Uarg=Uf)
+            extras["flash_S2048_us_per_layer_step"] = round(ms * 1000.0 / n_x, 3)
+            del wf
+
+    launches_per_step = 2
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "mode": args.mode, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "n_k": int(inp.lengths.max()),
+                   "tile": w.tile, "S": w.S, "kv_dtype": w.dtype, "accumulate": "f32",
+                   "parallelism": f"replicas{dist.world}",
+                   "l2": f"rotating {nrot} K/V copies, {nrot * per_copy / 2**20:.0f} MiB >= 4x L2 "
+                         f"({l2 / 2**20:.0f} MiB)",
+                   "timing": f"CUDA graphs of {args.graph_steps} calls, CUDA events on the launching stream"},
+        "hbm_gbs": round(bm["total"] / (per_step_us * 1e-6) / 1e9, 1),
+        "algorithmic_bytes_per_step": bm["total"],
+        "v_row_fraction": round(bm["v_rows"] / max(1, w.num_kv_heads * int(inp.lengths.sum())), 6)
+        if args.mode != "exact" else None,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "extras": extras,
+    }
+    if dist.rank == 0 and dist.world == 1:
+        res["cpu_baseline"] = cpu_baseline(inp, args.mode, w.S, args.cpu_seconds)
+    return res
+
+
+# ----------------------------------------------------------------------------- the oracle on the host
+
+
+def _oracle_problem(inp):
+    """float64 K/V per (sequence, KV head), prepared once outside any timing."""
+    w = inp.workload
+    kv = {}
+    for b in range(w.batch):
+        Kb, Vb = inp.k_f32(b), inp.v_f32(b)
+        for g in range(w.num_kv_heads):
+            kv[(b, g)] = (np.ascontiguousarray(Kb[:, g, :], dtype=np.float64),
+                          np.ascontiguousarray(Vb[:, g, :], dtype=np.float64))
+    return kv
+
+
+def _oracle_head(oracle, inp, kv, mode, S, b, h):
+    w = inp.workload
+    K, V = kv[(b, h // w.group)]
+    qh = np.ascontiguousarray(inp.q[b, h], dtype=np.float64)
+    U = float(inp.U[0, b, h])
+    if mode == "prop":
+        oracle.prop_head(qh, K, V, S, U, w.tile, want_F=False)
+    elif mode == "flash":
+        oracle.flash_head(qh, K, V, S, U, w.tile)
+    else:
+        oracle.exact_head(qh, K, V)
+
+
+def cpu_baseline(inp, mode, S, seconds):
+    """The oracle (single-threaded C, float64) on whole layer-steps until `seconds` pass."""
+    import oracle
+
+    oracle.build()
+    w = inp.workload
+    kv = _oracle_problem(inp)
+    heads = [(b, h) for b in range(w.batch) for h in range(w.num_q_heads)]
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        for b, h in heads:
+            _oracle_head(oracle, inp, kv, mode, S, b, h)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(el * 1e6 / n, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole layer-steps of {w.name} ({len(heads)} query heads), {mode}, "
+                      f"single-threaded C float64 oracle, {el:.1f} s", "cpu": _cpu_name()}
+
+
+def _cpu_name():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+def run_reference(args):
+    """Reference arm: the oracle on the host cores; one step = one query head."""
+    import oracle
+    from synthetic import generate, get_workload
+
+    w = get_workload(args.workload)
+    if args.S:
+        w = w.with_(S=args.S)
+    elif args.mode == "flash" and args.workload.startswith("llama8b"):
+        w = w.with_(S=2048)
+    inp = generate(w)
+    oracle.build()
+    kv = _oracle_problem(inp)
+    heads = [(b, h) for b in range(w.batch) for h in range(w.num_q_heads)]
+    for i in range(args.warmup):
+        _oracle_head(oracle, inp, kv, args.mode, w.S, *heads[i % len(heads)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_head(oracle, inp, kv, args.mode, w.S, *heads[i % len(heads)])
+    el = time.perf_counter() - t0
+    per_head_us = el * 1e6 / args.steps
+    value = per_head_us * len(heads)
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el * 1000 / args.steps, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "mode": args.mode, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "n_k": int(inp.lengths.max()),
+                   "tile": w.tile, "S": w.S, "kv_dtype": w.dtype},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step one query head of {w.name} ({args.mode}); value scaled by the "
+                                   f"{len(heads)} heads of a layer-step", "cpu": _cpu_name()},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    dist = Dist()
+    if args.gpus != dist.world and dist.world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {dist.world}")
+    res = run_ours(args, dist)
+    if dist.rank == 0:
+        print(json.dumps(res), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+/*
+ * santa_decode.h -- C ABI of the GB300 (sm_103a) stochastic sparse decode-attention library.
+ *
+ * One decode step of attention for a batch of sequences with a GQA-shared,
+ * token-major K/V cache, in three modes:
+ *
+ *   santa_decode_prop   S2ANTA-prop: a split-KV pass computes the logits
+ *                       x = q.k / sqrt(d) of every key, stashes the
+ *                       exponentiated scores and one partition sum Z_tile per
+ *                       tile; a reducer forms Z = sum Z_tile and places the S
+ *                       systematic thresholds U + m/S on the global CDF, so a
+ *                       tile's budget S_tile is the number of thresholds in its
+ *                       CDF interval (0 for low-mass tiles, which read no V);
+ *                       a second pass searches the stashed in-tile CDF for each
+ *                       threshold and averages the chosen V rows:
+ *                       out = (1/S) sum_m V[J_m].
+ *                       ("Stochastic Sparse Attention for Memory-Bound
+ *                       Inference", paper notes, Key designs 1 and 2.)
+ *   santa_decode_flash  S2ANTA-flash: every tile draws S_loc = ceil(S / T_b)
+ *                       systematic samples from its own scores as if it held
+ *                       all the mass; a merge rescales the tile estimates by
+ *                       Z_tile / Z.  (Same notes, Key design 3.)
+ *   exact_decode        exact split-KV decode attention, sum_i A_i V_i, with a
+ *                       log-sum-exp merge of the tiles (the dense comparison
+ *                       point; same notes, Related work: FlashDecoding).
+ *
+ * The logit scale is 1/sqrt(d) ("Double-P: Hierarchical Top-P Sparse Attention
+ * for Long-Context LLMs", paper review, Stage 1, Eq. 3).  A temperature is
+ * folded into q by the caller.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Shapes: B = batch, Hq query heads, Hkv KV heads (Hq % Hkv == 0; query head h
+ * reads KV head h / (Hq / Hkv)), d = head_dim, L_b = length of sequence b,
+ * T_b = ceil(L_b / tile) tiles, Tmax = ceil(max_len / tile).
+ *
+ * Layouts (all row-major, contiguous, device memory, 16-byte aligned):
+ *   q          [B][Hq][d]                 dtype
+ *   k, v       [total_tokens][Hkv][d]     dtype; sequence b owns rows
+ *                                         kv_indptr[b] .. kv_indptr[b+1]-1
+ *   kv_indptr  [B+1]   int64              non-decreasing, kv_indptr[B] <= total_tokens,
+ *                                         every L_b <= max_len
+ *   U          [B][Hq] float32            sampling offsets, each in [0, 1/S)
+ *   out        [B][Hq][d] float32         written entirely by every call
+ *
+ * Ownership: every buffer belongs to the caller.  The library allocates no
+ * device memory on the call path; its scratch lives in `workspace` (device,
+ * 256-byte aligned, at least santa_workspace_size() bytes), which carries no
+ * state from one call to the next.  Calls are asynchronous on `stream`; results
+ * are valid once the stream has reached the call's end.  Two calls may run
+ * concurrently only with distinct workspaces and outputs.
+ *
+ * Errors: host-side validation returns a status before anything is enqueued
+ * (nothing is written).  Inconsistent device data (a bad kv_indptr entry, an
+ * offset outside [0, 1/S)) cannot be seen from the host: the kernels treat such
+ * a sequence as empty (zeros out) or clamp the offset, and OR a bit into
+ * dbg->error_flags when that pointer is given.  No kernel traps.
+ */
+#ifndef SANTA_DECODE_H
+#define SANTA_DECODE_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA stream and event handles, declared without the CUDA headers
+ * (layout-compatible with cudaStream_t / cudaEvent_t). */
+typedef struct CUstream_st *santa_stream_t;
+typedef struct CUevent_st *santa_event_t;
+
+/* Status codes. */
+enum {
+    SANTA_OK = 0,
+    SANTA_INVALID_ARG = 1,          /* a null pointer, a bad size or a misaligned buffer */
+    SANTA_UNSUPPORTED = 2,          /* head_dim, GQA group or dtype not built */
+    SANTA_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < santa_workspace_size() */
+    SANTA_CUDA_ERROR = 4,           /* a CUDA launch or runtime call failed */
+    SANTA_DEVICE_CHECK = 5          /* santa_read_device_error found a flag set */
+};
+
+/* Element types of q, k and v (out is always float32). */
+enum { SANTA_F32 = 0, SANTA_BF16 = 1 };
+
+/* Modes, for santa_workspace_size. */
+enum { SANTA_MODE_PROP = 0, SANTA_MODE_FLASH = 1, SANTA_MODE_EXACT = 2 };
+
+/* Bits of the device error word (dbg->error_flags). */
+enum {
+    SANTA_ERR_INDPTR = 1u,   /* kv_indptr entry out of order / range: sequence treated as empty */
+    SANTA_ERR_OFFSET = 2u,   /* U outside [0, 1/S) or NaN: clamped into range */
+    SANTA_ERR_TIMEOUT = 4u   /* a bounded wait for an asynchronous copy gave up */
+};
+
+typedef struct {
+    int batch;               /* B >= 0 (B = 0 is a no-op) */
+    int num_q_heads;         /* Hq >= 1 */
+    int num_kv_heads;        /* Hkv >= 1, Hq / Hkv in {1, 2, 4, 8} */
+    int head_dim;            /* d in {64, 128} */
+    long long total_tokens;  /* rows of the K/V cache, >= kv_indptr[B] */
+    int max_len;             /* upper bound on every L_b (sizes the grid and workspace) */
+    int tile;                /* keys per tile: a power of two in [32, 1024] */
+    int S;                   /* samples per (sequence, query head), 1 <= S <= 2^20;
+                                ignored by exact_decode */
+    int dtype;               /* SANTA_F32 or SANTA_BF16 */
+} santa_problem;
+
+/* Optional outputs for inspection and timing; every pointer may be NULL.
+ * Entries for tiles t >= T_b of a sequence are left untouched. */
+typedef struct {
+    float *tile_m;           /* [B][Hq][Tmax] max logit of each tile */
+    float *tile_z;           /* [B][Hq][Tmax] sum of exp(x - tile_m) over the tile */
+    int *tile_count;         /* [B][Hq][Tmax] prop: S_tile; flash: S_loc of the tile */
+    int *sample_idx;         /* prop:  [B][Hq][S], key index within the sequence of
+                                       sample m (thresholds in increasing order);
+                                flash: [B][Hq][Tmax][sample_stride], the first
+                                       min(S_loc, sample_stride) samples of each tile */
+    int sample_stride;       /* flash only: row length of sample_idx */
+    unsigned int *error_flags;   /* device word; kernels OR SANTA_ERR_* bits into it */
+    santa_event_t main_begin;    /* recorded on `stream` right before / after the */
+    santa_event_t main_end;      /* mode's dominant kernel (prop pass 1, flash tile,
+                                    exact tile), for timing that kernel alone */
+} santa_debug;
+
+/*
+ * Bytes of workspace `mode` needs for problem *p.  Host only; enqueues nothing.
+ * Returns SANTA_OK, SANTA_INVALID_ARG or SANTA_UNSUPPORTED.
+ */
+int santa_workspace_size(const santa_problem *p, int mode, size_t *bytes);
+
+/*
+ * S2ANTA-prop decode (paper notes, Key designs 1-2).
+ * q, k, v, kv_indptr, U, out, workspace: device pointers as described above.
+ * Two kernels on `stream`: pass 1 (scores, stash, tile records) and pass 2
+ * (reducer over the T_b tile records, per-tile systematic search, V gather,
+ * deterministic combine).  Returns a status; see the conventions above.
+ */
+int santa_decode_prop(const santa_problem *p, const void *q, const void *k, const void *v,
+                      const long long *kv_indptr, const float *U, float *out,
+                      void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                      santa_stream_t stream);
+
+/*
+ * S2ANTA-flash decode (paper notes, Key design 3): S_loc = ceil(S / T_b)
+ * samples per tile with the shared offset U * S / S_loc, then a merge with
+ * weights Z_tile / Z.  Same arguments as santa_decode_prop.
+ */
+int santa_decode_flash(const santa_problem *p, const void *q, const void *k, const void *v,
+                       const long long *kv_indptr, const float *U, float *out,
+                       void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                       santa_stream_t stream);
+
+/*
+ * Exact split-KV decode: out = sum_i softmax(x)_i V_i, reading all of K and V.
+ * Same arguments as santa_decode_prop without U (p->S is ignored).
+ */
+int exact_decode(const santa_problem *p, const void *q, const void *k, const void *v,
+                 const long long *kv_indptr, float *out,
+                 void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                 santa_stream_t stream);
+
+/*
+ * Waits for `stream`, copies the device error word to *flags and clears it.
+ * Returns SANTA_OK if it was zero, SANTA_DEVICE_CHECK if a bit was set,
+ * SANTA_INVALID_ARG / SANTA_CUDA_ERROR otherwise.
+ */
+int santa_read_device_error(unsigned int *error_flags, santa_stream_t stream, unsigned int *flags);
+
+/* A static, human-readable name for a status code. */
+const char *santa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SANTA_DECODE_H */

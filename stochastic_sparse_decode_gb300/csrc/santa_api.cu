@@ -1,0 +1,297 @@
+// santa_api.cu -- the C entry points declared in santa_decode.h: argument
+// validation, workspace layout, TMA descriptors for the K/V cache, launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "santa_launch.h"
+
+using namespace santa;
+
+namespace {
+
+constexpr long long kMaxTokens = (1LL << 31) - 4096;  // TMA row coordinates are int32
+constexpr int kMaxS = 1 << 20;
+
+__global__ void zero_out_kernel(float *out, size_t n) {
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
+        out[i] = 0.f;
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Layout {
+    int Tmax = 0, nsplit = 0;
+    size_t rec_m = 0, rec_z = 0, stash = 0, partial = 0, tickets = 0, total = 0;
+};
+
+int check_problem(const santa_problem *p, int mode) {
+    if (!p) return SANTA_INVALID_ARG;
+    if (mode < SANTA_MODE_PROP || mode > SANTA_MODE_EXACT) return SANTA_INVALID_ARG;
+    if (p->batch < 0 || p->batch > 65535) return SANTA_INVALID_ARG;
+    if (p->num_q_heads < 1 || p->num_q_heads > 65535 || p->num_kv_heads < 1 || p->num_kv_heads > 65535)
+        return SANTA_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return SANTA_INVALID_ARG;
+    const int G = p->num_q_heads / p->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return SANTA_UNSUPPORTED;
+    if (p->head_dim != 64 && p->head_dim != 128) return SANTA_UNSUPPORTED;
+    if (p->dtype != SANTA_F32 && p->dtype != SANTA_BF16) return SANTA_UNSUPPORTED;
+    if (!is_pow2(p->tile) || p->tile < 32 || p->tile > 1024) return SANTA_INVALID_ARG;
+    if (mode != SANTA_MODE_EXACT && (p->S < 1 || p->S > kMaxS)) return SANTA_INVALID_ARG;
+    if (p->max_len < 0 || p->total_tokens < 0 || p->total_tokens > kMaxTokens) return SANTA_INVALID_ARG;
+    return SANTA_OK;
+}
+
+// Workspace regions of one call, each 256-byte aligned.  Sizes are computed in
+// double first so that absurd shapes are rejected instead of wrapping around.
+int make_layout(const santa_problem *p, int mode, Layout *L) {
+    const int Tmax = (p->max_len + p->tile - 1) / p->tile;
+    const double B = p->batch, Hq = p->num_q_heads, D = p->head_dim;
+    const double nrec = B * Hq * Tmax;
+    const int nsplit = (Tmax + kTilesPerSplit - 1) / kTilesPerSplit;
+    double est = 2 * nrec * 4;
+    if (mode == SANTA_MODE_PROP)
+        est += Hq * double(p->total_tokens) * 4 + B * Hq * nsplit * D * 4 + B * Hq * 4;
+    else
+        est += nrec * D * 4;
+    if (est > 1e15) return SANTA_INVALID_ARG;
+
+    const size_t n_rec = size_t(p->batch) * p->num_q_heads * size_t(Tmax);
+    size_t off = 0;
+    L->Tmax = Tmax;
+    L->nsplit = nsplit;
+    L->rec_m = off;
+    off += align256(n_rec * 4);
+    L->rec_z = off;
+    off += align256(n_rec * 4);
+    if (mode == SANTA_MODE_PROP) {
+        L->stash = off;
+        off += align256(size_t(p->num_q_heads) * size_t(p->total_tokens) * 4);
+        L->partial = off;
+        off += align256(size_t(p->batch) * p->num_q_heads * size_t(nsplit) * p->head_dim * 4);
+        L->tickets = off;
+        off += align256(size_t(p->batch) * p->num_q_heads * 4);
+    } else {
+        L->partial = off;
+        off += align256(n_rec * p->head_dim * 4);
+    }
+    L->total = off > 256 ? off : 256;
+    return SANTA_OK;
+}
+
+int smem_check(const santa_problem *p, int mode) {
+    const int G = p->num_q_heads / p->num_kv_heads;
+    size_t need = 0;
+    if (mode == SANTA_MODE_PROP)
+        need = prop_pass1_smem(p->dtype, p->head_dim, G, p->tile);
+    else if (mode == SANTA_MODE_FLASH)
+        need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
+    else
+        need = exact_tile_smem(p->dtype, p->head_dim, G, p->tile);
+    if (mode == SANTA_MODE_PROP) {
+        const size_t s2 = prop_pass2_smem(p->head_dim, p->tile);
+        if (s2 > need) need = s2;
+    }
+    return need <= 227 * 1024 ? SANTA_OK : SANTA_UNSUPPORTED;
+}
+
+// ---- TMA descriptors of a [total_tokens][Hkv][d] cache, box = d x 1 x kChunk rows
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void *base;
+    int dtype, d, hkv, dev;
+    long long rows;
+    bool operator==(const MapKey &o) const {
+        return base == o.base && dtype == o.dtype && d == o.d && hkv == o.hkv && dev == o.dev && rows == o.rows;
+    }
+};
+
+bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long long rows) {
+    static std::mutex mu;
+    static MapKey keys[32];
+    static CUtensorMap maps[32];
+    static int used = 0, next = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const MapKey key{base, dtype, d, hkv, dev, rows};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == key) {
+            *map = maps[i];
+            return true;
+        }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const int es = dtype == SANTA_BF16 ? 2 : 4;
+    const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(rows)};
+    const cuuint64_t strides[2] = {cuuint64_t(d) * es, cuuint64_t(hkv) * d * es};
+    const cuuint32_t box[3] = {cuuint32_t(d), 1u, cuuint32_t(kChunk)};
+    const cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUtensorMap m;
+    const CUresult r = enc(&m, dtype == SANTA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                           3, const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    keys[next] = key;
+    maps[next] = m;
+    next = (next + 1) % 32;
+    if (used < 32) ++used;
+    *map = m;
+    return true;
+}
+
+int run(int mode, const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
+        const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+        santa_stream_t stream_) {
+    int st = check_problem(p, mode);
+    if (st != SANTA_OK) return st;
+    if (p->batch == 0) return SANTA_OK;
+    if (!q || !k || !v || !kv_indptr || !out || !workspace) return SANTA_INVALID_ARG;
+    if (mode != SANTA_MODE_EXACT && !U) return SANTA_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(kv_indptr, 8) ||
+        !aligned(workspace, 256) || (U && !aligned(U, 4)))
+        return SANTA_INVALID_ARG;
+    if (dbg && dbg->sample_stride < 0) return SANTA_INVALID_ARG;
+    Layout L;
+    st = make_layout(p, mode, &L);
+    if (st != SANTA_OK) return st;
+    if (workspace_bytes < L.total) return SANTA_WORKSPACE_TOO_SMALL;
+    st = smem_check(p, mode);
+    if (st != SANTA_OK) return st;
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const size_t n_out = size_t(p->batch) * p->num_q_heads * p->head_dim;
+    if (L.Tmax == 0 || p->total_tokens == 0) {  // no sequence can hold a key
+        zero_out_kernel<<<(unsigned)((n_out + 255) / 256 < 1024 ? (n_out + 255) / 256 : 1024), 256, 0, stream>>>(out, n_out);
+        return cudaGetLastError() == cudaSuccess ? SANTA_OK : SANTA_CUDA_ERROR;
+    }
+
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    Params prm = {};
+    prm.B = p->batch;
+    prm.Hq = p->num_q_heads;
+    prm.Hkv = p->num_kv_heads;
+    prm.G = p->num_q_heads / p->num_kv_heads;
+    prm.D = p->head_dim;
+    prm.tile = p->tile;
+    prm.S = mode == SANTA_MODE_EXACT ? 1 : p->S;
+    prm.Tmax = L.Tmax;
+    prm.max_len = p->max_len;
+    prm.total_tokens = p->total_tokens;
+    prm.scale = float(1.0 / std::sqrt(double(p->head_dim)));
+    prm.q = q;
+    prm.k = k;
+    prm.v = v;
+    prm.kv_indptr = kv_indptr;
+    prm.U = U;
+    prm.out = out;
+    prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
+    prm.rec_z = reinterpret_cast<float *>(ws + L.rec_z);
+    prm.stash = mode == SANTA_MODE_PROP ? reinterpret_cast<float *>(ws + L.stash) : nullptr;
+    prm.partial = reinterpret_cast<float *>(ws + L.partial);
+    prm.tickets = mode == SANTA_MODE_PROP ? reinterpret_cast<unsigned int *>(ws + L.tickets) : nullptr;
+    prm.nsplit = L.nsplit;
+    prm.tiles_per_split = kTilesPerSplit;
+    Timing tm;
+    if (dbg) {
+        prm.dbg_tile_m = dbg->tile_m;
+        prm.dbg_tile_z = dbg->tile_z;
+        prm.dbg_count = dbg->tile_count;
+        prm.dbg_idx = dbg->sample_idx;
+        prm.dbg_stride = dbg->sample_stride;
+        prm.err = dbg->error_flags;
+        tm.begin = reinterpret_cast<cudaEvent_t>(dbg->main_begin);
+        tm.end = reinterpret_cast<cudaEvent_t>(dbg->main_end);
+    }
+
+    CUtensorMap kmap, vmap;
+    if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens)) return SANTA_CUDA_ERROR;
+    cudaError_t e;
+    if (mode == SANTA_MODE_PROP) {
+        e = launch_prop(prm, p->dtype, kmap, stream, tm);
+    } else if (mode == SANTA_MODE_FLASH) {
+        e = launch_flash(prm, p->dtype, kmap, stream, tm);
+    } else {
+        if (!kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens)) return SANTA_CUDA_ERROR;
+        e = launch_exact(prm, p->dtype, kmap, vmap, stream, tm);
+    }
+    if (e == cudaErrorInvalidValue) return SANTA_UNSUPPORTED;
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SANTA_CUDA_ERROR;
+    return SANTA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int santa_workspace_size(const santa_problem *p, int mode, size_t *bytes) {
+    if (!bytes) return SANTA_INVALID_ARG;
+    const int st = check_problem(p, mode);
+    if (st != SANTA_OK) return st;
+    Layout L;
+    const int s2 = make_layout(p, mode, &L);
+    if (s2 != SANTA_OK) return s2;
+    *bytes = L.total;
+    return SANTA_OK;
+}
+
+int santa_decode_prop(const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
+                      const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                      santa_stream_t stream) {
+    return run(SANTA_MODE_PROP, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
+}
+
+int santa_decode_flash(const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
+                       const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                       santa_stream_t stream) {
+    return run(SANTA_MODE_FLASH, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
+}
+
+int exact_decode(const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
+                 float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
+    return run(SANTA_MODE_EXACT, p, q, k, v, kv_indptr, nullptr, out, workspace, workspace_bytes, dbg, stream);
+}
+
+int santa_read_device_error(unsigned int *error_flags, santa_stream_t stream_, unsigned int *flags) {
+    if (!error_flags || !flags) return SANTA_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    unsigned int h = 0;
+    if (cudaMemcpyAsync(&h, error_flags, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemsetAsync(error_flags, 0, sizeof(h), stream) != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess)
+        return SANTA_CUDA_ERROR;
+    *flags = h;
+    return h ? SANTA_DEVICE_CHECK : SANTA_OK;
+}
+
+const char *santa_status_string(int status) {
+    switch (status) {
+        case SANTA_OK: return "ok";
+        case SANTA_INVALID_ARG: return "invalid argument";
+        case SANTA_UNSUPPORTED: return "unsupported head_dim, GQA group or dtype";
+        case SANTA_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case SANTA_CUDA_ERROR: return "CUDA error";
+        case SANTA_DEVICE_CHECK: return "device check flagged an input";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,289 @@
+// santa_common.cuh -- device helpers shared by the decode kernels (sm_103a).
+//
+// PTX wrappers for the asynchronous-copy machinery (mbarrier, TMA tensor loads,
+// programmatic dependent launch), warp/block scans and reductions, bf16
+// unpacking, and the parameter block every kernel receives.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "santa_decode.h"
+
+namespace santa {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kChunk = 32;       // keys per TMA copy
+constexpr int kStages = 4;       // TMA copies in flight per tile CTA
+constexpr int kTileWarps = 4;    // warps of a tile CTA
+constexpr int kPass2Warps = 8;   // warps of a prop pass-2 CTA
+constexpr int kMergeThreads = 128;
+constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
+
+enum Mode { kProp = 0, kFlash = 1, kExact = 2 };
+
+// Everything a kernel needs; built by the host entry points.
+struct Params {
+    int B, Hq, Hkv, G, D, tile, S, Tmax, max_len;
+    long long total_tokens;
+    float scale;  // 1/sqrt(d)
+    const void *q, *k, *v;
+    const long long *kv_indptr;
+    const float *U;
+    float *out;
+    // workspace
+    float *rec_m, *rec_z;  // [B][Hq][Tmax] tile max logit, tile partition sum
+    float *stash;          // prop: [Hq][total_tokens] exp(x - m_t)
+    float *partial;        // prop: [B][Hq][nsplit][D]; flash/exact: [B][Hq][Tmax][D]
+    unsigned int *tickets; // prop: [B][Hq]
+    int nsplit, tiles_per_split;
+    // optional debug outputs
+    float *dbg_tile_m, *dbg_tile_z;
+    int *dbg_count, *dbg_idx;
+    int dbg_stride;
+    unsigned int *err;
+};
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes initialised barriers visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier shared-memory accesses before later async-proxy writes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete; gives up after kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
+    return true;
+}
+
+// 3-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now; and, in that kernel, wait until this one's memory is visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------------ element types
+
+// K/V/q storage: bf16 is carried as its 16-bit pattern.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T>
+__device__ __forceinline__ float to_float(T x);
+template <>
+__device__ __forceinline__ float to_float<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_float<uint16_t>(uint16_t x) { return __uint_as_float(uint32_t(x) << 16); }
+
+// A 16-byte vector of elements as float pairs (4 pairs of bf16, 2 pairs of fp32).
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<uint16_t> {
+    static constexpr int kPairs = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float2 *o) {
+        o[0] = make_float2(bf16_lo(r.x), bf16_hi(r.x));
+        o[1] = make_float2(bf16_lo(r.y), bf16_hi(r.y));
+        o[2] = make_float2(bf16_lo(r.z), bf16_hi(r.z));
+        o[3] = make_float2(bf16_lo(r.w), bf16_hi(r.w));
+    }
+};
+template <>
+struct Vec16<float> {
+    static constexpr int kPairs = 2;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float2 *o) {
+        o[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+        o[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+    }
+};
+
+// A lane's slice of one V row: D/32 consecutive elements at element lane*D/32.
+template <typename T, int D>
+struct RowSlice {
+    static constexpr int kElems = D / 32;
+    static constexpr int kBytes = kElems * int(sizeof(T));  // 4, 8 or 16
+    float v[kElems];
+    __device__ __forceinline__ void load(const T *row, int lane) {
+        const unsigned char *p = reinterpret_cast<const unsigned char *>(row) + lane * kBytes;
+        if constexpr (kBytes == 4) {
+            uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(p));
+            unpack_words(&w);
+        } else if constexpr (kBytes == 8) {
+            uint2 w = __ldg(reinterpret_cast<const uint2 *>(p));
+            uint32_t a[2] = {w.x, w.y};
+            unpack_words(a);
+        } else {
+            uint4 w = __ldg(reinterpret_cast<const uint4 *>(p));
+            uint32_t a[4] = {w.x, w.y, w.z, w.w};
+            unpack_words(a);
+        }
+    }
+    __device__ __forceinline__ void load_shared(const unsigned char *row, int lane) {
+        const unsigned char *p = row + lane * kBytes;
+        if constexpr (kBytes == 4) {
+            uint32_t w = *reinterpret_cast<const uint32_t *>(p);
+            unpack_words(&w);
+        } else if constexpr (kBytes == 8) {
+            uint2 w = *reinterpret_cast<const uint2 *>(p);
+            uint32_t a[2] = {w.x, w.y};
+            unpack_words(a);
+        } else {
+            uint4 w = *reinterpret_cast<const uint4 *>(p);
+            uint32_t a[4] = {w.x, w.y, w.z, w.w};
+            unpack_words(a);
+        }
+    }
+    __device__ __forceinline__ void unpack_words(const uint32_t *w) {
+        if constexpr (sizeof(T) == 2) {
+#pragma unroll
+            for (int i = 0; i < kElems / 2; ++i) {
+                v[2 * i] = bf16_lo(w[i]);
+                v[2 * i + 1] = bf16_hi(w[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kElems; ++i) v[i] = __uint_as_float(w[i]);
+        }
+    }
+};
+
+// ------------------------------------------------------------------ reductions / scans
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_max_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+// Inclusive prefix sum across the warp (Hillis-Steele, fixed order).
+__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += u;
+    }
+    return v;
+}
+
+// Chunked inclusive scan of exp-scores over one tile by one warp: element i of
+// the tile sits at lane i % 32 of step i / 32, and each step adds the previous
+// step's total.  Both the producer of the stash and its reader run exactly this
+// sequence of additions, so they obtain bit-identical prefixes.
+struct TileScan {
+    float carry = 0.f;
+    int last_pos = -1;  // last index with a positive score
+    __device__ __forceinline__ float step(float e, int idx, int lane) {
+        const float v = warp_inclusive_scan(e, lane) + carry;
+        carry = __shfl_sync(kFull, v, 31);
+        if (e > 0.f) last_pos = idx;
+        return v;
+    }
+    __device__ __forceinline__ void finish() { last_pos = warp_max_int(last_pos); }
+};
+
+// Smallest i in [0, len) with P[i] > target (P non-decreasing), else last_pos.
+// Negative or NaN targets count as 0, so a zero-mass key is never returned.
+// (last_pos < 0 only if every score of the tile is NaN; key 0 keeps the read in bounds.)
+__device__ __forceinline__ int cdf_search(const float *P, int len, float target, int last_pos) {
+    if (last_pos < 0) return 0;
+    if (!(target > 0.f)) target = 0.f;
+    int lo = 0, hi = len;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (P[mid] > target)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo < last_pos ? lo : last_pos;
+}
+
+// ------------------------------------------------------------------ validation
+
+__device__ __forceinline__ void raise_flag(const Params &p, unsigned bit) {
+    if (p.err) atomicOr(p.err, bit);
+}
+
+// Start and length of sequence b; an inconsistent kv_indptr entry gives an
+// empty sequence and raises SANTA_ERR_INDPTR.
+__device__ __forceinline__ int seq_bounds(const Params &p, int b, long long *start) {
+    const long long s = p.kv_indptr[b], e = p.kv_indptr[b + 1];
+    if (s < 0 || e < s || e > p.total_tokens || e - s > (long long)p.max_len) {
+        raise_flag(p, SANTA_ERR_INDPTR);
+        *start = 0;
+        return 0;
+    }
+    *start = s;
+    return int(e - s);
+}
+
+// Offset U of (b, h), clamped into [0, 1/S) (SANTA_ERR_OFFSET if it was not).
+__device__ __forceinline__ float load_offset(const Params &p, int b, int h) {
+    float u = p.U[b * p.Hq + h];
+    if (!(u >= 0.f) || double(u) * double(p.S) >= 1.0) {
+        raise_flag(p, SANTA_ERR_OFFSET);
+        u = (u >= 0.f) ? nextafterf(1.0f / float(p.S), 0.f) : 0.f;
+        while (double(u) * double(p.S) >= 1.0) u = nextafterf(u, 0.f);
+    }
+    return u;
+}
+
+}  // namespace santa

@@ -1,0 +1,30 @@
+// santa_exact.cu -- launch of the exact split-KV decode: tile kernel then merge.
+#include "santa_launch.h"
+#include "santa_pass2.cuh"
+#include "santa_tile.cuh"
+
+namespace santa {
+
+size_t exact_tile_smem(int dtype, int d, int g, int tile) {
+    size_t bytes = 0;
+    SANTA_DISPATCH(dtype, d, g, { bytes = TileSmem<T, D, G, kExact>::bytes(tile); return cudaSuccess; });
+    return bytes;
+}
+
+cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                         cudaStream_t stream, const Timing &tm) {
+    return SANTA_DISPATCH(dtype, p.D, p.G, {
+        auto k1 = tile_kernel<kExact, T, D, G>;
+        auto k2 = merge_kernel<kExact, D>;
+        const size_t s1 = TileSmem<T, D, G, kExact>::bytes(p.tile);
+        cudaError_t e = ensure_smem(k1, s1);
+        if (e != cudaSuccess) return e;
+        if (tm.begin) cudaEventRecord(tm.begin, stream);
+        e = launch_kernel(k1, dim3(p.Tmax, p.Hkv, p.B), dim3(kTileWarps * 32), s1, stream, false, kmap, vmap, p);
+        if (e != cudaSuccess) return e;
+        if (tm.end) cudaEventRecord(tm.end, stream);
+        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, true, p);
+    });
+}
+
+}  // namespace santa

@@ -1,0 +1,93 @@
+// santa_launch.h -- host-side glue between the C entry points and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "santa_common.cuh"
+
+namespace santa {
+
+constexpr int kTilesPerSplit = 16;  // prop pass 2: tiles owned by one CTA
+
+// Launches `kern` on `stream`; with `pdl` the kernel may start while the
+// previous kernel in the stream drains (programmatic dependent launch).
+template <typename... Exp, typename... Act>
+cudaError_t launch_kernel(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Act &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Act &&>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device.
+template <typename K>
+cudaError_t ensure_smem(K kern, size_t bytes) {
+    static size_t done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (bytes <= 48 * 1024 || bytes <= done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (e == cudaSuccess) done[dev] = bytes;
+    return e;
+}
+
+struct Timing {
+    cudaEvent_t begin = nullptr, end = nullptr;
+};
+
+// Mode launchers (one translation unit each).  `dtype` is SANTA_F32/SANTA_BF16.
+cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
+cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
+cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                         cudaStream_t stream, const Timing &tm);
+
+// Shared-memory needs, for validation on the host.
+size_t prop_pass1_smem(int dtype, int D, int G, int tile);
+size_t prop_pass2_smem(int D, int tile);
+size_t flash_tile_smem(int dtype, int D, int G, int tile);
+size_t exact_tile_smem(int dtype, int D, int G, int tile);
+
+}  // namespace santa
+
+// Expands the body (the variadic tail) with T (element type), D and G bound to the runtime
+// (dtype, d, g); evaluates to cudaErrorInvalidValue for combinations not built.
+#define SANTA_DISPATCH(dtype, d, g, ...)                                        \
+    [&]() -> cudaError_t {                                                       \
+        if ((dtype) == SANTA_BF16) {                                             \
+            using T = uint16_t;                                                  \
+            SANTA_DISPATCH_DG(d, g, __VA_ARGS__)                                        \
+        } else {                                                                 \
+            using T = float;                                                     \
+            SANTA_DISPATCH_DG(d, g, __VA_ARGS__)                                        \
+        }                                                                        \
+    }()
+#define SANTA_DISPATCH_DG(d, g, ...)                                            \
+    if ((d) == 128) {                                                            \
+        constexpr int D = 128;                                                   \
+        SANTA_DISPATCH_G(g, __VA_ARGS__)                                                \
+    } else if ((d) == 64) {                                                      \
+        constexpr int D = 64;                                                    \
+        SANTA_DISPATCH_G(g, __VA_ARGS__)                                                \
+    }                                                                            \
+    return cudaErrorInvalidValue;
+#define SANTA_DISPATCH_G(g, ...)                                                \
+    switch (g) {                                                                 \
+        case 1: { constexpr int G = 1; __VA_ARGS__ }                                    \
+        case 2: { constexpr int G = 2; __VA_ARGS__ }                                    \
+        case 4: { constexpr int G = 4; __VA_ARGS__ }                                    \
+        case 8: { constexpr int G = 8; __VA_ARGS__ }                                    \
+        default: return cudaErrorInvalidValue;                                   \
+    }

@@ -1,0 +1,63 @@
+"""A convenience wrapper: owns the problem description and the workspaces.
+
+    dec = Decoder(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                  total_tokens=32768, max_len=32768, tile=256, S=128, dtype="bf16")
+    out = dec("prop", q, k, v, kv_indptr, U)
+
+Workspaces are allocated once per mode with torch (device memory only); each
+call is one C-ABI call on the current stream.  Debug buffers can be requested
+to inspect tile records, budgets and sampled indices.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import MODES, Debug, decode, make_problem, workspace_size
+
+
+class Decoder:
+    def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, total_tokens, max_len, tile, S, dtype,
+                 device=None):
+        self.problem = make_problem(batch, num_q_heads, num_kv_heads, head_dim, total_tokens, max_len, tile, S,
+                                    dtype)
+        self.device = torch.device(device if device is not None else "cuda")
+        self.Tmax = -(-max_len // tile) if max_len > 0 else 0
+        self._ws = {}
+
+    def workspace(self, mode: str) -> torch.Tensor:
+        if mode not in self._ws:
+            n = workspace_size(self.problem, MODES[mode])
+            self._ws[mode] = torch.empty(n, dtype=torch.uint8, device=self.device)
+        return self._ws[mode]
+
+    def debug_buffers(self, mode: str, sample_stride: int = 0):
+        """(Debug struct, dict of the tensors it points to)."""
+        p = self.problem
+        B, Hq, T = p.batch, p.num_q_heads, max(self.Tmax, 1)
+        dev = self.device
+        bufs = {
+            "tile_m": torch.full((B, Hq, T), float("nan"), device=dev),
+            "tile_z": torch.full((B, Hq, T), float("nan"), device=dev),
+            "tile_count": torch.full((B, Hq, T), -1, dtype=torch.int32, device=dev),
+            "error_flags": torch.zeros(1, dtype=torch.int32, device=dev),
+        }
+        if mode == "prop":
+            bufs["sample_idx"] = torch.full((B, Hq, p.S), -1, dtype=torch.int32, device=dev)
+        elif mode == "flash":
+            bufs["sample_idx"] = torch.full((B, Hq, T, max(sample_stride, 1)), -1, dtype=torch.int32, device=dev)
+        dbg = Debug()
+        dbg.tile_m = bufs["tile_m"].data_ptr()
+        dbg.tile_z = bufs["tile_z"].data_ptr()
+        dbg.tile_count = bufs["tile_count"].data_ptr()
+        dbg.sample_idx = bufs["sample_idx"].data_ptr() if "sample_idx" in bufs else None
+        dbg.sample_stride = int(sample_stride) if mode == "flash" else 0
+        dbg.error_flags = bufs["error_flags"].data_ptr()
+        return dbg, bufs
+
+    def __call__(self, mode, q, k, v, kv_indptr, U=None, out=None, debug=None, stream=None) -> torch.Tensor:
+        p = self.problem
+        if out is None:
+            out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=torch.float32, device=self.device)
+        decode(mode, p, q, k, v, kv_indptr, U, out, self.workspace(mode), debug, stream)
+        return out

@@ -14,4 +14,6 @@ from .workloads import (  # noqa: F401
     float32_to_bf16_bits,
     generate,
     get_workload,
+    max_length,
+    to_torch,
 )

@@ -36,6 +36,7 @@ __all__ = [
     "generate",
     "float32_to_bf16_bits",
     "bf16_bits_to_float32",
+    "to_torch",
 ]
 
 
@@ -54,6 +55,7 @@ class Workload:
     dtype: str  # "f32" or "bf16"
     length: int = 0  # fixed length of every sequence (ignored if length_range set)
     length_range: tuple[int, int] | None = None  # ragged: UniformInt[lo, hi]
+    lengths: tuple[int, ...] = ()  # explicit per-sequence lengths (edge cases)
     planted_per_head: int = 0  # fixed count of planted keys per query head
     planted_fraction: float = 0.0  # or a fraction of each sequence per KV head
     sinks: int = 0
@@ -163,12 +165,23 @@ for _n in (4096, 8192, 16384, 32768, 65536, 131072):
     )
 
 
+def max_length(w: Workload) -> int:
+    if w.lengths:
+        return max(w.lengths)
+    if w.length_range is not None:
+        return w.length_range[1]
+    return w.length
+
+
 def get_workload(name: str, **overrides) -> Workload:
     w = WORKLOADS[name]
     return w.with_(**overrides) if overrides else w
 
 
 def _lengths(w: Workload, rng: np.random.Generator) -> np.ndarray:
+    if w.lengths:
+        assert len(w.lengths) == w.batch
+        return np.asarray(w.lengths, dtype=np.int64)
     if w.length_range is not None:
         lo, hi = w.length_range
         return rng.integers(lo, hi + 1, size=w.batch, dtype=np.int64)
@@ -243,3 +256,21 @@ def generate(w: Workload, instance: int = 0, n_offsets: int | None = None) -> In
     U = draw_offsets(w.S, (n_off, B, Hq), np.random.Generator(np.random.PCG64(s_u)))
     return Inputs(workload=w, seed=seed, lengths=lengths, kv_indptr=indptr, q=q, k=k, v=v, U=U,
                   q_native=q_native.reshape(B, Hq, d))
+
+
+def to_torch(inp: Inputs, device="cuda", U_index: int = 0):
+    """Device tensors (q, k, v, kv_indptr, U) of an instance, in the workload dtype."""
+    import torch
+
+    def native(a):
+        if inp.workload.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+
+    return (
+        native(inp.q_native).to(device),
+        native(inp.k).to(device),
+        native(inp.v).to(device),
+        torch.from_numpy(inp.kv_indptr).to(device),
+        torch.from_numpy(np.ascontiguousarray(inp.U[U_index])).to(device),
+    )

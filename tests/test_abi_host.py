@@ -1,0 +1,169 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before enqueuing anything.
+
+No call here reaches a kernel launch: every argument set fails host validation
+(the device pointers are never dereferenced on the host).
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "santa_decode.h")
+
+
+@pytest.fixture(scope="module")
+def sd():
+    from stochastic_sparse_decode_gb300.build import build
+
+    build()
+    import stochastic_sparse_decode_gb300 as sd
+
+    return sd
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("santa_decode_prop", "santa_decode_flash", "exact_decode", "santa_workspace_size",
+              "santa_read_device_error", "santa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(sd):
+    names = _declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", sd.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    lib = sd.lib()
+    for n in names:
+        assert getattr(lib, n) is not None
+    assert set(sd.EXPORTS) == set(names)
+
+
+def _north_star(sd, **kw):
+    args = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, total_tokens=32768, max_len=32768,
+                tile=256, S=128, dtype="bf16")
+    args.update(kw)
+    return sd.make_problem(**args)
+
+
+def test_workspace_layout_matches_the_byte_model(sd):
+    """prop: 2 tile-record arrays, the fp32 score stash [Hq][n_k], the pass-2
+    partials [B][Hq][ceil(T/16)][d] and one ticket per head, each rounded up to 256 B."""
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    p = _north_star(sd)
+    T = 32768 // 256
+    rec = r(1 * 32 * T * 4)
+    prop = 2 * rec + r(32 * 32768 * 4) + r(1 * 32 * (T // 16) * 128 * 4) + r(32 * 4)
+    assert sd.workspace_size(p, sd.MODE_PROP) == prop
+    flash = 2 * rec + r(1 * 32 * T * 128 * 4)
+    assert sd.workspace_size(p, sd.MODE_FLASH) == flash
+    assert sd.workspace_size(p, sd.MODE_EXACT) == flash
+    # ragged tail: T = ceil(max_len / tile)
+    p = _north_star(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
+    T = 8
+    assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 96, "UNSUPPORTED"),
+    ("dtype", 7, "UNSUPPORTED"),
+    ("num_q_heads", 24, "UNSUPPORTED"),   # group of 3
+    ("num_q_heads", 30, "INVALID_ARG"),   # not a multiple of Hkv
+    ("tile", 48, "INVALID_ARG"),
+    ("tile", 2048, "INVALID_ARG"),
+    ("tile", 16, "INVALID_ARG"),
+    ("S", 0, "INVALID_ARG"),
+    ("S", (1 << 20) + 1, "INVALID_ARG"),
+    ("batch", -1, "INVALID_ARG"),
+    ("max_len", -5, "INVALID_ARG"),
+    ("total_tokens", 1 << 40, "INVALID_ARG"),
+])
+def test_bad_problems_are_rejected(sd, field, value, status):
+    p = _north_star(sd)
+    setattr(p, field, value)
+    n = ctypes.c_size_t(0)
+    st = sd.lib().santa_workspace_size(ctypes.byref(p), sd.MODE_PROP, ctypes.byref(n))
+    assert st == getattr(sd, status)
+
+
+def test_exact_ignores_S(sd):
+    p = _north_star(sd, S=0)
+    assert sd.workspace_size(p, sd.MODE_EXACT) > 0
+    with pytest.raises(sd.SantaError):
+        sd.workspace_size(p, sd.MODE_PROP)
+
+
+class _FakeTensor:
+    """A device address that is never dereferenced (validation fails first)."""
+
+    def __init__(self, addr, nbytes=0):
+        self.addr, self.nbytes = addr, nbytes
+
+    def data_ptr(self):
+        return self.addr
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+
+def _call_prop(sd, p, q=0x10000, k=0x20000, v=0x30000, ind=0x40000, U=0x50000, out=0x60000, ws=0x100000,
+               ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = sd.workspace_size(p, sd.MODE_PROP)
+    t = lambda a: None if a is None else _FakeTensor(a)  # noqa: E731
+    try:
+        sd.santa_decode_prop(p, t(q), t(k), t(v), t(ind), t(U), t(out), _FakeTensor(ws, ws_bytes), stream=0)
+    except sd.SantaError as e:
+        return e.status
+    return sd.OK
+
+
+def test_null_misaligned_and_small_workspace_are_rejected(sd):
+    p = _north_star(sd)
+    assert _call_prop(sd, p, q=None) == sd.INVALID_ARG
+    assert _call_prop(sd, p, U=None) == sd.INVALID_ARG
+    assert _call_prop(sd, p, out=None) == sd.INVALID_ARG
+    assert _call_prop(sd, p, k=0x20008) == sd.INVALID_ARG      # K not 16-byte aligned
+    assert _call_prop(sd, p, ind=0x40004) == sd.INVALID_ARG    # kv_indptr not 8-byte aligned
+    assert _call_prop(sd, p, ws=0x100080) == sd.INVALID_ARG    # workspace not 256-byte aligned
+    need = sd.workspace_size(p, sd.MODE_PROP)
+    assert _call_prop(sd, p, ws_bytes=need - 1) == sd.WORKSPACE_TOO_SMALL
+    # batch 0 is a no-op that touches nothing
+    assert _call_prop(sd, _north_star(sd, batch=0), q=None, k=None) == sd.OK
+
+
+def test_exact_needs_no_offsets(sd):
+    p = _north_star(sd)
+    ws = sd.workspace_size(p, sd.MODE_EXACT)
+    with pytest.raises(sd.SantaError) as e:
+        sd.exact_decode(p, _FakeTensor(0x10000), _FakeTensor(0x20000), _FakeTensor(0x30000), None,
+                        _FakeTensor(0x60000), _FakeTensor(0x100000, ws), stream=0)
+    assert e.value.status == sd.INVALID_ARG  # kv_indptr is required
+
+
+def test_status_strings(sd):
+    for s in range(6):
+        assert sd.status_string(s) and sd.status_string(s) != "unknown status"
+    assert sd.status_string(99) == "unknown status"
+
+
+def test_missing_library_fails_loudly(monkeypatch, sd):
+    monkeypatch.setattr(sd, "_lib", None)
+    monkeypatch.setattr(sd, "LIB_PATH", "/nonexistent/libsanta_decode.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        sd.lib()
