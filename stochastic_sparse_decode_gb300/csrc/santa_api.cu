@@ -234,7 +234,7 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
         if (!kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens)) return SANTA_CUDA_ERROR;
         e = launch_exact(prm, p->dtype, kmap, vmap, stream, tm);
     }
-    if (e == cudaErrorInvalidValue) return SANTA_UNSUPPORTED;
+    if (e == cudaErrorNotSupported) return SANTA_UNSUPPORTED;
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SANTA_CUDA_ERROR;
     return SANTA_OK;
 }

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "santa_common.cuh"
 
 namespace santa {
@@ -30,17 +32,27 @@ cudaError_t launch_kernel(void (*kern)(Exp...), dim3 grid, dim3 block, size_t sm
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Act &&>(args)...);
 }
 
-// Raises a kernel's dynamic shared-memory limit once per device.
+// Raises a kernel's dynamic shared-memory limit (once per kernel and device).
 template <typename K>
 cudaError_t ensure_smem(K kern, size_t bytes) {
-    static size_t done[64] = {};
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    struct Entry {
+        const void *fn;
+        int dev;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int used = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (bytes <= 48 * 1024 || bytes <= done[dev]) return cudaSuccess;
+    const void *fn = reinterpret_cast<const void *>(kern);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (done[i].fn == fn && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
-    if (e == cudaSuccess) done[dev] = bytes;
+    if (e == cudaSuccess && used < 256) done[used++] = Entry{fn, dev, bytes};
     return e;
 }
 
@@ -63,7 +75,7 @@ size_t exact_tile_smem(int dtype, int D, int G, int tile);
 }  // namespace santa
 
 // Expands the body (the variadic tail) with T (element type), D and G bound to the runtime
-// (dtype, d, g); evaluates to cudaErrorInvalidValue for combinations not built.
+// (dtype, d, g); evaluates to cudaErrorNotSupported for combinations not built.
 #define SANTA_DISPATCH(dtype, d, g, ...)                                        \
     [&]() -> cudaError_t {                                                       \
         if ((dtype) == SANTA_BF16) {                                             \
@@ -82,12 +94,12 @@ size_t exact_tile_smem(int dtype, int D, int G, int tile);
         constexpr int D = 64;                                                    \
         SANTA_DISPATCH_G(g, __VA_ARGS__)                                                \
     }                                                                            \
-    return cudaErrorInvalidValue;
+    return cudaErrorNotSupported;
 #define SANTA_DISPATCH_G(g, ...)                                                \
     switch (g) {                                                                 \
         case 1: { constexpr int G = 1; __VA_ARGS__ }                                    \
         case 2: { constexpr int G = 2; __VA_ARGS__ }                                    \
         case 4: { constexpr int G = 4; __VA_ARGS__ }                                    \
         case 8: { constexpr int G = 8; __VA_ARGS__ }                                    \
-        default: return cudaErrorInvalidValue;                                   \
+        default: return cudaErrorNotSupported;                                   \
     }
