@@ -160,6 +160,35 @@ int exact_decode(const santa_problem *p, const void *q, const void *k, const voi
                  void *workspace, size_t workspace_bytes, const santa_debug *dbg,
                  santa_stream_t stream);
 
+/* Size of the library's built-in scratch array (see santa_decode_prop_static_scratch). */
+#define SANTA_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * santa_decode_prop without a workspace argument, for callers that cannot
+ * allocate device memory: e.g. a plugin inside a host program that owns every
+ * device allocation through its own pool and gives plugins no allocator, or a
+ * C caller on a path where cudaMalloc's implicit synchronisation is not allowed.
+ * (This entry point has no counterpart in the paper; it is a packaging choice.)
+ *
+ * The scratch is a file-scope device array of SANTA_STATIC_SCRATCH_BYTES (16 MiB)
+ * that every GPU loading this library holds until the process exits.  Problems
+ * whose prop workspace (santa_workspace_size with SANTA_MODE_PROP) exceeds that
+ * size are rejected with SANTA_WORKSPACE_TOO_SMALL before anything is enqueued;
+ * roughly, num_q_heads * total_tokens must stay below about 4 million.  The other
+ * arguments, their layouts, ownership and errors are those of santa_decode_prop.
+ * Nothing is allocated: not by this call, and not by any routine it calls.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Every call shares the one array, which keeps the last
+ * call's contents; what must start at zero is reset inside each call, so results
+ * never depend on an earlier call.  Calls whose kernels overlap on the GPU
+ * (unordered streams or threads) race on the array: order them.
+ */
+int santa_decode_prop_static_scratch(const santa_problem *p, const void *q, const void *k, const void *v,
+                                     const long long *kv_indptr, const float *U, float *out,
+                                     const santa_debug *dbg, santa_stream_t stream);
+
 /*
  * Waits for `stream`, copies the device error word to *flags and clears it.
  * Returns SANTA_OK if it was zero, SANTA_DEVICE_CHECK if a bit was set,

@@ -29,6 +29,7 @@ EXPORTS = (
     "santa_decode_flash",
     "exact_decode",
     "santa_read_device_error",
+    "santa_decode_prop_static_scratch",
     "santa_status_string",
 )
 
@@ -88,6 +89,7 @@ def lib() -> ctypes.CDLL:
         for name in ("santa_decode_prop", "santa_decode_flash"):
             getattr(L, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.exact_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
+        L.santa_decode_prop_static_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, Dp, vp]
         L.santa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint)]
         L.santa_status_string.argtypes = [ctypes.c_int]
         L.santa_status_string.restype = ctypes.c_char_p
@@ -155,6 +157,19 @@ def exact_decode(problem, q, k, v, kv_indptr, out, workspace, debug=None, stream
     """Exact split-KV decode: see santa_decode.h."""
     _call("exact_decode", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(out)],
           workspace, debug, stream)
+
+
+STATIC_SCRATCH_BYTES = 16 << 20  # SANTA_STATIC_SCRATCH_BYTES
+
+
+def santa_decode_prop_static_scratch(problem, q, k, v, kv_indptr, U, out, debug=None, stream=None):
+    """S2ANTA-prop decode with the library's built-in 16 MiB scratch array instead of a
+    caller workspace, for callers that cannot allocate device memory (see santa_decode.h)."""
+    dbg = ctypes.byref(debug) if debug is not None else None
+    st = lib().santa_decode_prop_static_scratch(ctypes.byref(problem), _ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr),
+                                                _ptr(U), _ptr(out), dbg, _stream(stream))
+    if st != OK:
+        raise SantaError(st, "santa_decode_prop_static_scratch")
 
 
 def santa_read_device_error(error_flags, stream=None) -> int:
