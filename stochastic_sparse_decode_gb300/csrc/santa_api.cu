@@ -25,8 +25,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Layout {
-    int Tmax = 0, nsplit = 0;
-    size_t rec_m = 0, rec_z = 0, stash = 0, partial = 0, tickets = 0, total = 0;
+    int Tmax = 0, nsplit = 0, tps = 0;
+    size_t rec_m = 0, rec_z = 0, stash = 0, partial = 0, total = 0;
 };
 
 int check_problem(const santa_problem *p, int mode) {
@@ -43,6 +43,7 @@ int check_problem(const santa_problem *p, int mode) {
     if (!is_pow2(p->tile) || p->tile < 32 || p->tile > 1024) return SANTA_INVALID_ARG;
     if (mode != SANTA_MODE_EXACT && (p->S < 1 || p->S > kMaxS)) return SANTA_INVALID_ARG;
     if (p->max_len < 0 || p->total_tokens < 0 || p->total_tokens > kMaxTokens) return SANTA_INVALID_ARG;
+    if ((p->max_len + p->tile - 1) / p->tile > 65535) return SANTA_INVALID_ARG;  // tiles are a grid dimension
     return SANTA_OK;
 }
 
@@ -52,10 +53,9 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     const int Tmax = (p->max_len + p->tile - 1) / p->tile;
     const double B = p->batch, Hq = p->num_q_heads, D = p->head_dim;
     const double nrec = B * Hq * Tmax;
-    const int nsplit = (Tmax + kTilesPerSplit - 1) / kTilesPerSplit;
     double est = 2 * nrec * 4;
     if (mode == SANTA_MODE_PROP)
-        est += Hq * double(p->total_tokens) * 4 + B * Hq * nsplit * D * 4 + B * Hq * 4;
+        est += Hq * double(p->total_tokens) * 4;
     else
         est += nrec * D * 4;
     if (est > 1e15) return SANTA_INVALID_ARG;
@@ -63,7 +63,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     const size_t n_rec = size_t(p->batch) * p->num_q_heads * size_t(Tmax);
     size_t off = 0;
     L->Tmax = Tmax;
-    L->nsplit = nsplit;
+    prop_split(Tmax, &L->nsplit, &L->tps);
     L->rec_m = off;
     off += align256(n_rec * 4);
     L->rec_z = off;
@@ -71,10 +71,6 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     if (mode == SANTA_MODE_PROP) {
         L->stash = off;
         off += align256(size_t(p->num_q_heads) * size_t(p->total_tokens) * 4);
-        L->partial = off;
-        off += align256(size_t(p->batch) * p->num_q_heads * size_t(nsplit) * p->head_dim * 4);
-        L->tickets = off;
-        off += align256(size_t(p->batch) * p->num_q_heads * 4);
     } else {
         L->partial = off;
         off += align256(n_rec * p->head_dim * 4);
@@ -93,13 +89,14 @@ int smem_check(const santa_problem *p, int mode) {
     else
         need = exact_tile_smem(p->dtype, p->head_dim, G, p->tile);
     if (mode == SANTA_MODE_PROP) {
-        const size_t s2 = prop_pass2_smem(p->head_dim, p->tile);
+        const size_t s2 = prop_pass2_smem(p->head_dim, p->tile, (p->max_len + p->tile - 1) / p->tile);
         if (s2 > need) need = s2;
     }
     return need <= 227 * 1024 ? SANTA_OK : SANTA_UNSUPPORTED;
 }
 
-// ---- TMA descriptors of a [total_tokens][Hkv][d] cache, box = d x 1 x kChunk rows
+// ---- TMA descriptors of a [total_tokens][Hkv][d] cache: boxes of 128 bytes of one
+// KV head's row x box_rows rows, with the 128-byte swizzle the kernels expect
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -117,21 +114,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 struct MapKey {
     const void *base;
-    int dtype, d, hkv, dev;
+    int dtype, d, hkv, dev, box_rows;
     long long rows;
     bool operator==(const MapKey &o) const {
-        return base == o.base && dtype == o.dtype && d == o.d && hkv == o.hkv && dev == o.dev && rows == o.rows;
+        return base == o.base && dtype == o.dtype && d == o.d && hkv == o.hkv && dev == o.dev &&
+               box_rows == o.box_rows && rows == o.rows;
     }
 };
 
-bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long long rows) {
+bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long long rows, int box_rows) {
     static std::mutex mu;
     static MapKey keys[32];
     static CUtensorMap maps[32];
     static int used = 0, next = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    const MapKey key{base, dtype, d, hkv, dev, rows};
+    const MapKey key{base, dtype, d, hkv, dev, box_rows, rows};
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (keys[i] == key) {
@@ -143,12 +141,12 @@ bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long 
     const int es = dtype == SANTA_BF16 ? 2 : 4;
     const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(hkv), cuuint64_t(rows)};
     const cuuint64_t strides[2] = {cuuint64_t(d) * es, cuuint64_t(hkv) * d * es};
-    const cuuint32_t box[3] = {cuuint32_t(d), 1u, cuuint32_t(kChunk)};
+    const cuuint32_t box[3] = {cuuint32_t(128 / es), 1u, cuuint32_t(box_rows)};
     const cuuint32_t estride[3] = {1u, 1u, 1u};
     CUtensorMap m;
     const CUresult r = enc(&m, dtype == SANTA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                            3, const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     keys[next] = key;
@@ -181,7 +179,8 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const size_t n_out = size_t(p->batch) * p->num_q_heads * p->head_dim;
     if (L.Tmax == 0 || p->total_tokens == 0) {  // no sequence can hold a key
-        zero_out_kernel<<<(unsigned)((n_out + 255) / 256 < 1024 ? (n_out + 255) / 256 : 1024), 256, 0, stream>>>(out, n_out);
+        const unsigned blocks = unsigned((n_out + 255) / 256 < 1024 ? (n_out + 255) / 256 : 1024);
+        zero_out_kernel<<<blocks, 256, 0, stream>>>(out, n_out);
         return cudaGetLastError() == cudaSuccess ? SANTA_OK : SANTA_CUDA_ERROR;
     }
 
@@ -207,10 +206,9 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
     prm.rec_z = reinterpret_cast<float *>(ws + L.rec_z);
     prm.stash = mode == SANTA_MODE_PROP ? reinterpret_cast<float *>(ws + L.stash) : nullptr;
-    prm.partial = reinterpret_cast<float *>(ws + L.partial);
-    prm.tickets = mode == SANTA_MODE_PROP ? reinterpret_cast<unsigned int *>(ws + L.tickets) : nullptr;
+    prm.partial = mode == SANTA_MODE_PROP ? nullptr : reinterpret_cast<float *>(ws + L.partial);
     prm.nsplit = L.nsplit;
-    prm.tiles_per_split = kTilesPerSplit;
+    prm.tiles_per_split = L.tps;
     Timing tm;
     if (dbg) {
         prm.dbg_tile_m = dbg->tile_m;
@@ -224,14 +222,17 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     }
 
     CUtensorMap kmap, vmap;
-    if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens)) return SANTA_CUDA_ERROR;
+    if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows)) return SANTA_CUDA_ERROR;
     cudaError_t e;
     if (mode == SANTA_MODE_PROP) {
-        e = launch_prop(prm, p->dtype, kmap, stream, tm);
+        CUtensorMap kmap32;
+        if (!kv_map(&kmap32, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32)) return SANTA_CUDA_ERROR;
+        e = launch_prop(prm, p->dtype, kmap, kmap32, stream, tm);
     } else if (mode == SANTA_MODE_FLASH) {
         e = launch_flash(prm, p->dtype, kmap, stream, tm);
     } else {
-        if (!kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens)) return SANTA_CUDA_ERROR;
+        if (!kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
+            return SANTA_CUDA_ERROR;
         e = launch_exact(prm, p->dtype, kmap, vmap, stream, tm);
     }
     if (e == cudaErrorNotSupported) return SANTA_UNSUPPORTED;

@@ -14,10 +14,10 @@
 namespace santa {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kChunk = 32;       // keys per TMA copy
-constexpr int kStages = 4;       // TMA copies in flight per tile CTA
 constexpr int kTileWarps = 4;    // warps of a tile CTA
+constexpr int kWarpRows = 64;    // K/V rows per TMA chunk of one warp (2 per lane)
 constexpr int kPass2Warps = 8;   // warps of a prop pass-2 CTA
+constexpr int kMaxSplit = 8;     // prop pass 2: CTAs per head = size of its cluster
 constexpr int kMergeThreads = 128;
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
 
@@ -35,9 +35,8 @@ struct Params {
     // workspace
     float *rec_m, *rec_z;  // [B][Hq][Tmax] tile max logit, tile partition sum
     float *stash;          // prop: [Hq][total_tokens] exp(x - m_t)
-    float *partial;        // prop: [B][Hq][nsplit][D]; flash/exact: [B][Hq][Tmax][D]
-    unsigned int *tickets; // prop: [B][Hq]
-    int nsplit, tiles_per_split;
+    float *partial;        // flash/exact: [B][Hq][Tmax][D] tile estimates
+    int nsplit, tiles_per_split;  // prop pass 2: CTAs (one cluster) per head, tiles per CTA
     // optional debug outputs
     float *dbg_tile_m, *dbg_tile_z;
     int *dbg_count, *dbg_idx;
@@ -105,6 +104,21 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+
+// Distributed shared memory of a thread-block cluster: the address of `p` (a
+// shared-memory location of this CTA) in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Hardware cluster barrier, split in its two halves (every thread of every CTA
+// of the cluster executes both, outside divergent code).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue now; and, in that kernel, wait until this one's memory is visible.

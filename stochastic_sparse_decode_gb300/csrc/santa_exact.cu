@@ -20,10 +20,10 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
         cudaError_t e = ensure_smem(k1, s1);
         if (e != cudaSuccess) return e;
         if (tm.begin) cudaEventRecord(tm.begin, stream);
-        e = launch_kernel(k1, dim3(p.Tmax, p.Hkv, p.B), dim3(kTileWarps * 32), s1, stream, false, kmap, vmap, p);
+        e = launch_kernel(k1, dim3(p.Hkv, p.Tmax, p.B), dim3(kTileWarps * 32), s1, stream, false, 0, kmap, vmap, p);
         if (e != cudaSuccess) return e;
         if (tm.end) cudaEventRecord(tm.end, stream);
-        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, true, p);
+        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, true, 0, p);
     });
 }
 

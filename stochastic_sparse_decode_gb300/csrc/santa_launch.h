@@ -10,25 +10,44 @@
 
 namespace santa {
 
-constexpr int kTilesPerSplit = 16;  // prop pass 2: tiles owned by one CTA
+// prop pass 2: CTAs per head (a cluster of at most kMaxSplit) and tiles per CTA
+// (a multiple of the warp count, at least two per warp).
+inline void prop_split(int Tmax, int *nsplit, int *tps) {
+    int n = (Tmax + 2 * kPass2Warps - 1) / (2 * kPass2Warps);
+    n = n < 1 ? 1 : (n > kMaxSplit ? kMaxSplit : n);
+    int per = (Tmax + n - 1) / n;
+    per = (per + kPass2Warps - 1) / kPass2Warps * kPass2Warps;
+    *nsplit = n;
+    *tps = per < kPass2Warps ? kPass2Warps : per;
+}
 
 // Launches `kern` on `stream`; with `pdl` the kernel may start while the
 // previous kernel in the stream drains (programmatic dependent launch).
+// With cluster_x > 0 the grid's x dimension is cut into thread-block clusters of that size.
 template <typename... Exp, typename... Act>
 cudaError_t launch_kernel(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
-                          Act &&...args) {
+                          int cluster_x, Act &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int n = 0;
     if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
+    if (cluster_x > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = unsigned(cluster_x);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Act &&>(args)...);
 }
 
@@ -61,14 +80,16 @@ struct Timing {
 };
 
 // Mode launchers (one translation unit each).  `dtype` is SANTA_F32/SANTA_BF16.
-cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
+// kmap64 / kmap32: K descriptors with boxes of 64 rows (tile kernel) and 32 rows (streaming kernel).
+cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap64, const CUtensorMap &kmap32,
+                        cudaStream_t stream, const Timing &tm);
 cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
 cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          cudaStream_t stream, const Timing &tm);
 
 // Shared-memory needs, for validation on the host.
 size_t prop_pass1_smem(int dtype, int D, int G, int tile);
-size_t prop_pass2_smem(int D, int tile);
+size_t prop_pass2_smem(int D, int tile, int Tmax);
 size_t flash_tile_smem(int dtype, int D, int G, int tile);
 size_t exact_tile_smem(int dtype, int D, int G, int tile);
 

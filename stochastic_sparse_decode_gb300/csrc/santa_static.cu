@@ -11,10 +11,10 @@
 // The entry point runs the same kernels as santa_decode_prop, with this array
 // as their workspace; it allocates nothing itself and calls no allocating
 // routine.  All calls share the array and it keeps the last call's contents;
-// the only scratch that must start at zero (the per-head completion tickets of
-// pass 2) is reset by pass 1 of every call, so a call never depends on what an
-// earlier call left behind.  Calls whose kernels overlap on the GPU (different
-// streams, or threads that do not order their streams) race on the array.
+// nothing in it has to start at zero -- every call writes each scratch value
+// before reading it -- so a call never depends on what an earlier call left
+// behind.  Calls whose kernels overlap on the GPU (different streams, or
+// threads that do not order their streams) race on the array.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -1,17 +1,23 @@
 // santa_tile.cuh -- the split-KV tile kernel shared by the three modes.
 //
 // One CTA owns one (sequence b, KV head, tile t) and all G query heads of that
-// KV head's GQA group, so each K row is read once for G heads.  The tile's K
-// rows (and, for the exact mode, then its V rows) stream through a ring of
-// kStages shared-memory slots filled by 3-D TMA copies of kChunk rows each;
-// 4 warps compute the G dot products per key while later chunks are in flight.
+// KV head's GQA group, so each K row is read once for G heads.  The CTA's four
+// warps split the tile into 64-row chunks (chunk w of every 256-key round goes
+// to warp w); each warp streams its chunks through its own shared-memory slots,
+// filled by 3-D TMA boxes of 64 rows x 128 bytes with the 128-byte swizzle, and
+// waits on its own mbarriers -- no CTA-wide barrier in the streaming loop.
 //
-// After the scores x = q.k / sqrt(d) of the tile are in shared memory, each
-// head (one warp per head) forms the tile's max m_t and the exponentiated
-// scores e_i = exp(x_i - m_t), and scans them once (TileScan) to get
-// z_t = sum e_i -- the tile's partition sum Z_tile on the m_t scale
-// ("Stochastic Sparse Attention for Memory-Bound Inference", paper notes,
-// Key design 2: exponentiated scores plus one Z_tile per tile).  Then:
+// A lane owns whole keys (rows l and l + 32 of its warp's chunk), so a dot
+// product never crosses lanes: for each 16-byte column vector j of the row the
+// lane reads its two rows' vectors (the swizzle makes a column read by 32 lanes
+// conflict-free), widens bf16 to fp32 and accumulates with packed fp32 FMA
+// against q, which all lanes read from shared memory as a broadcast.
+//
+// With the scores x = q.k / sqrt(d) of the tile in shared memory, one warp per
+// query head forms the tile's max m_t, the exponentiated scores
+// e_i = exp(x_i - m_t) and their sum z_t -- the tile's partition sum Z_tile on
+// the m_t scale ("Stochastic Sparse Attention for Memory-Bound Inference", paper
+// notes, Key design 2: exponentiated scores plus one Z_tile per tile).  Then:
 //
 //   kProp   writes e to the score stash and (m_t, z_t) to the tile records;
 //           the reducer and the sampling happen in pass 2.
@@ -19,51 +25,69 @@
 //           U_t = U S / S_loc, on the tile's own CDF (its prefix of e divided
 //           by z_t), gather-averages the chosen V rows into the tile estimate
 //           and writes it with (m_t, z_t) for the merge (Key design 3).
-//   kExact  streams the tile's V rows and accumulates sum_i e_i V_i for the
-//           log-sum-exp merge (exact split-KV decode).
+//   kExact  streams the tile's V rows through the same slots and accumulates
+//           sum_i e_i V_i for the log-sum-exp merge (exact split-KV decode).
 #pragma once
 
 #include "santa_common.cuh"
 
 namespace santa {
 
+constexpr int kBoxBytes = kWarpRows * 128;           // one TMA box: 64 rows x 128 bytes
+constexpr int kRoundKeys = kTileWarps * kWarpRows;   // keys per round of the CTA
+
 template <typename T, int D>
 struct TileGeom {
     static constexpr int kES = int(sizeof(T));
     static constexpr int kRowBytes = D * kES;        // 128, 256 or 512
-    static constexpr int kVecs = kRowBytes / 16;     // 16-byte vectors per row
-    static constexpr int kVecsPerLane = kVecs / 8;   // 8 lanes share one key
-    static constexpr int kPairs = Vec16<T>::kPairs;  // float pairs per vector
-    static constexpr int kChunkBytes = kChunk * kRowBytes;
+    static constexpr int kBoxes = kRowBytes / 128;   // 128-byte column boxes per row
+    static constexpr int kBoxElems = 128 / kES;      // elements per box row
+    static constexpr int kEV = 16 / kES;             // elements per 16-byte vector
+    static constexpr int kPairs = kEV / 2;           // float pairs per 16-byte vector
+    static constexpr int kNJ = D / kEV;              // 16-byte vectors per row
+    static constexpr int kChunkBytes = kBoxes * kBoxBytes;
 };
 
-// Shared-memory layout of a tile CTA (identical on host and device).
+// Byte offset of 16-byte vector j of row r (0..63) in a chunk: box j/8, and
+// inside it the 128-byte swizzle (vector c of row r sits at c ^ (r mod 8)).
+__device__ __forceinline__ uint32_t swz(int r, int j) {
+    return uint32_t((j >> 3) * kBoxBytes + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+
+// Shared-memory layout of a tile CTA (identical on host and device).  Offsets
+// are from a 1024-byte aligned base; `bytes` includes the alignment slack.
 template <typename T, int D, int G, int MODE>
 struct TileSmem {
-    static constexpr size_t stage_off() { return 0; }
-    static constexpr size_t xs_off() { return size_t(kStages) * TileGeom<T, D>::kChunkBytes; }
-    static __host__ __device__ size_t bars_off(int tile) { return xs_off() + size_t(G) * tile * 4; }
-    static __host__ __device__ size_t red_off(int tile) { return bars_off(tile) + kStages * 8 + 16; }
+    static __host__ __device__ int nslot(int tile) { return tile > kRoundKeys ? 2 : 1; }
+    static __host__ __device__ size_t q_off(int tile) {
+        return size_t(kTileWarps) * nslot(tile) * TileGeom<T, D>::kChunkBytes;
+    }
+    static __host__ __device__ size_t xs_off(int tile) { return q_off(tile) + size_t(G) * D * 4; }
+    static __host__ __device__ size_t es_off(int tile) { return xs_off(tile) + size_t(G) * tile * 4; }
+    static __host__ __device__ size_t bars_off(int tile) {
+        return es_off(tile) + (MODE == kExact ? size_t(G) * tile * 4 : 0);
+    }
+    static __host__ __device__ size_t red_off(int tile) { return bars_off(tile) + kTileWarps * 2 * 8 + 16; }
     static __host__ __device__ size_t bytes(int tile) {
-        return red_off(tile) + (MODE == kExact ? size_t(kTileWarps) * G * D * 4 : 0);
+        return 1024 + red_off(tile) + (MODE == kExact ? size_t(kTileWarps) * G * D * 4 : 0);
     }
 };
 
 // Gather-average helper: adds V rows J (one per lane of `j`, the first n lanes)
-// of one KV head to the lane's slice accumulator, 8 loads in flight at a time.
+// of one KV head to the lane's slice accumulator, up to 16 loads in flight.
 template <typename T, int D>
 __device__ __forceinline__ void gather_rows(float (&acc)[D / 32], const T *vrow0, size_t row_stride, int j, int n,
                                             int lane) {
     constexpr int kE = D / 32;
-    for (int r0 = 0; r0 < n; r0 += 8) {
-        RowSlice<T, D> rows[8];
+    for (int r0 = 0; r0 < n; r0 += 16) {
+        RowSlice<T, D> rows[16];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int jr = __shfl_sync(kFull, j, r0 + r);
+        for (int r = 0; r < 16; ++r) {
+            const int jr = __shfl_sync(kFull, j, (r0 + r) & 31);
             if (r0 + r < n) rows[r].load(vrow0 + size_t(jr) * row_stride, lane);
         }
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 16; ++r)
             if (r0 + r < n) {
 #pragma unroll
                 for (int e = 0; e < kE; ++e) acc[e] += rows[r].v[e];
@@ -77,23 +101,36 @@ __global__ void __launch_bounds__(kTileWarps * 32)
     using Geo = TileGeom<T, D>;
     using Lay = TileSmem<T, D, G, MODE>;
     constexpr int kE = D / 32;
-    const int t = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // KV head fastest: the Hkv CTAs of one tile are scheduled together and read
+    // the same token rows, so each DRAM page is streamed by them at once.
+    const int kvh = blockIdx.x, t = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = p.tile;
     const int hq0 = kvh * G;
+    const int nslot = Lay::nslot(tile);
 
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *stage = smem + Lay::stage_off();
-    float *xs = reinterpret_cast<float *>(smem + Lay::xs_off());
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                            ~uintptr_t(1023));
+    float *qs = reinterpret_cast<float *>(smem + Lay::q_off(tile));
+    float *xs = reinterpret_cast<float *>(smem + Lay::xs_off(tile));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::bars_off(tile));
-    int *s_fail = reinterpret_cast<int *>(bars + kStages);
+    int *s_fail = reinterpret_cast<int *>(bars + kTileWarps * 2);
 
     // The dependent kernel (prop pass 2 / merge) may become resident as this grid drains;
     // it waits on pdl_wait() before touching anything written here.
     pdl_launch_dependents();
 
-    if constexpr (MODE == kProp) {
-        if (t == 0 && tid < G) p.tickets[size_t(b) * p.Hq + hq0 + tid] = 0u;
+    // q of the group's G heads: loads issued before the sequence bounds are known.
+    constexpr int kQPerThread = (G * D + kTileWarps * 32 - 1) / (kTileWarps * 32);
+    float qreg[kQPerThread];
+    {
+        const T *qb = static_cast<const T *>(p.q) + (size_t(b) * p.Hq + hq0) * D;
+#pragma unroll
+        for (int k = 0; k < kQPerThread; ++k) {
+            const int i = tid + k * kTileWarps * 32;
+            qreg[k] = i < G * D ? to_float<T>(qb[i]) : 0.f;
+        }
     }
 
     long long start;
@@ -103,128 +140,129 @@ __global__ void __launch_bounds__(kTileWarps * 32)
     const int k0 = t * tile;
     const int len = min(tile, L - k0);
     const long long tok0 = start + k0;
-    const int nk = (len + kChunk - 1) / kChunk;
-    const int nchunks = (MODE == kExact) ? 2 * nk : nk;
 
-    if (tid == 0) {
-        prefetch_tensormap(&kmap);
-        if (MODE == kExact) prefetch_tensormap(&vmap);
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-        s_fail[0] = 0;
+    // This warp's chunks: rounds r with keys 256 r + 64 warp < len (then, for the
+    // exact mode, the same rounds again for V).
+    const int nr = len > kWarpRows * warp ? (len - kWarpRows * warp + kRoundKeys - 1) / kRoundKeys : 0;
+    const int nch = (MODE == kExact) ? 2 * nr : nr;
+    unsigned char *wslots = smem + size_t(warp) * nslot * Geo::kChunkBytes;
+    uint64_t *wbars = bars + warp * 2;
+
+    if (lane == 0) {
+        for (int s = 0; s < nslot; ++s) mbar_init(&wbars[s], 1);
         fence_barrier_init();
     }
+    if (tid == 0) s_fail[0] = 0;
     __syncthreads();
 
-    // Chunk c < nk is K rows [32c, 32c+32) of the tile; c >= nk (exact) the same rows of V.
-    auto issue = [&](int c) {
-        const int slot = c % kStages;
-        const bool is_v = (MODE == kExact) && c >= nk;
-        const int row = int(tok0) + (is_v ? c - nk : c) * kChunk;
-        mbar_arrive_expect_tx(&bars[slot], Geo::kChunkBytes);
-        tma_load_3d(stage + slot * Geo::kChunkBytes, is_v ? &vmap : &kmap, &bars[slot], 0, kvh, row);
+    auto issue = [&](int c) {  // lane 0 only
+        const int slot = c % nslot;
+        const bool is_v = (MODE == kExact) && c >= nr;
+        const int row = int(tok0) + (is_v ? c - nr : c) * kRoundKeys + warp * kWarpRows;
+        unsigned char *dst = wslots + slot * Geo::kChunkBytes;
+        mbar_arrive_expect_tx(&wbars[slot], Geo::kChunkBytes);
+#pragma unroll
+        for (int bx = 0; bx < Geo::kBoxes; ++bx)
+            tma_load_3d(dst + bx * kBoxBytes, is_v ? &vmap : &kmap, &wbars[slot], bx * Geo::kBoxElems, kvh, row);
     };
     int issued = 0;
-    if (tid == 0) {
-        issued = min(kStages, nchunks);
+    if (lane == 0) {
+        issued = min(nslot, nch);
         for (int c = 0; c < issued; ++c) issue(c);
     }
     auto wait_chunk = [&](int c) {
         if (s_fail[0]) return;  // after a timeout nothing more is awaited
-        if (!mbar_wait(&bars[c % kStages], (c / kStages) & 1)) s_fail[0] = 1;
+        if (!mbar_wait(&wbars[c % nslot], (c / nslot) & 1)) s_fail[0] = 1;
     };
-    auto release_chunk = [&](int c) {  // call after a __syncthreads: every warp is done with slot c
-        if (tid == 0 && c + kStages < nchunks && !s_fail[0]) {
+    auto release_chunk = [&](int c) {  // every lane of the warp is done with chunk c
+        __syncwarp();
+        if (lane == 0 && c + nslot < nch && !s_fail[0]) {
             fence_proxy_async_smem();
-            issue(c + kStages);
-            issued = c + kStages + 1;
+            issue(c + nslot);
+            issued = c + nslot + 1;
         }
     };
 
-    // q of the G heads: this lane's 16-byte vectors l8, l8 + 8, ... of the row, as float pairs.
-    const int l8 = lane & 7, grp = lane >> 3;
-    float2 qv[G][Geo::kVecsPerLane * Geo::kPairs];
-    {
-        const T *qb = static_cast<const T *>(p.q) + (size_t(b) * p.Hq + hq0) * D;
+    // q, widened to fp32, in shared memory for broadcast reads.
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int i = 0; i < Geo::kVecsPerLane; ++i)
-#pragma unroll
-                for (int pp = 0; pp < Geo::kPairs; ++pp) {
-                    const int e = (l8 + 8 * i) * (2 * Geo::kPairs) + 2 * pp;
-                    qv[h][i * Geo::kPairs + pp] = make_float2(to_float<T>(qb[h * D + e]), to_float<T>(qb[h * D + e + 1]));
-                }
+    for (int k = 0; k < kQPerThread; ++k) {
+        const int i = tid + k * kTileWarps * 32;
+        if (i < G * D) qs[i] = qreg[k];
     }
+    __syncthreads();
 
-    // ---- scores: warp w takes keys 8w..8w+7 of each chunk, 8 lanes per key, two keys per pass
-    for (int c = 0; c < nk; ++c) {
-        wait_chunk(c);
-        const unsigned char *base = stage + (c % kStages) * Geo::kChunkBytes;
-        float dot[2][G];
+    // ---- scores of this warp's keys: lane owns rows `lane` and `lane + 32` of each chunk
+    for (int r = 0; r < nr; ++r) {
+        wait_chunk(r);
+        const unsigned char *base = wslots + (r % nslot) * Geo::kChunkBytes;
+        float2 acc0[G], acc1[G];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            const unsigned char *row = base + (warp * 8 + s * 4 + grp) * Geo::kRowBytes;
-            float2 acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < Geo::kVecsPerLane; ++i) {
-                const uint4 r = *reinterpret_cast<const uint4 *>(row + (l8 + 8 * i) * 16);
-                float2 kv[Geo::kPairs];
-                Vec16<T>::unpack(r, kv);
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int pp = 0; pp < Geo::kPairs; ++pp)
-                        acc[h] = __ffma2_rn(qv[h][i * Geo::kPairs + pp], kv[pp], acc[h]);
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) dot[s][h] = acc[h].x + acc[h].y;
+        for (int h = 0; h < G; ++h) {
+            acc0[h] = make_float2(0.f, 0.f);
+            acc1[h] = make_float2(0.f, 0.f);
         }
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
+        for (int j = 0; j < Geo::kNJ; ++j) {
+            const uint32_t o = swz(lane, j);
+            const uint4 ra = *reinterpret_cast<const uint4 *>(base + o);
+            const uint4 rb = *reinterpret_cast<const uint4 *>(base + o + 32 * 128);
+            float2 ka[Geo::kPairs], kb[Geo::kPairs];
+            Vec16<T>::unpack(ra, ka);
+            Vec16<T>::unpack(rb, kb);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float v = dot[s][h];
-                v += __shfl_xor_sync(kFull, v, 4);
-                v += __shfl_xor_sync(kFull, v, 2);
-                v += __shfl_xor_sync(kFull, v, 1);
-                dot[s][h] = v;
-            }
+                const float4 *qh = reinterpret_cast<const float4 *>(qs + h * D + j * Geo::kEV);
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            const int kidx = c * kChunk + warp * 8 + s * 4 + grp;
-            if (kidx < len) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-                    if (l8 == h) xs[h * tile + kidx] = dot[s][h] * p.scale;
+                for (int i = 0; i < Geo::kPairs / 2; ++i) {
+                    const float4 qq = qh[i];
+                    const float2 q0 = make_float2(qq.x, qq.y), q1 = make_float2(qq.z, qq.w);
+                    acc0[h] = __ffma2_rn(q0, ka[2 * i], acc0[h]);
+                    acc1[h] = __ffma2_rn(q0, kb[2 * i], acc1[h]);
+                    acc0[h] = __ffma2_rn(q1, ka[2 * i + 1], acc0[h]);
+                    acc1[h] = __ffma2_rn(q1, kb[2 * i + 1], acc1[h]);
+                }
             }
         }
-        __syncthreads();
-        release_chunk(c);
+        release_chunk(r);
+        const int key0 = r * kRoundKeys + warp * kWarpRows + lane;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            if (key0 < len) xs[h * tile + key0] = (acc0[h].x + acc0[h].y) * p.scale;
+            if (key0 + 32 < len) xs[h * tile + key0 + 32] = (acc1[h].x + acc1[h].y) * p.scale;
+        }
     }
+    __syncthreads();
 
     // ---- per-head tile statistics: m_t, e_i = exp(x_i - m_t), z_t (+ the flash sampler)
+    float *es = reinterpret_cast<float *>(smem + Lay::es_off(tile));  // exact: e as [key][G]
     for (int h = warp; h < G; h += kTileWarps) {
         float *xh = xs + h * tile;
         float m = -INFINITY;
         for (int i = lane; i < len; i += 32) m = fmaxf(m, xh[i]);
         m = warp_max(m);
+        float z;
         TileScan sc;
-        float *srow = nullptr;
-        if constexpr (MODE == kProp) srow = p.stash + size_t(hq0 + h) * p.total_tokens + tok0;
-        for (int i0 = 0; i0 < len; i0 += 32) {
-            const int i = i0 + lane;
-            const float e = (i < len) ? __expf(xh[i] - m) : 0.f;
-            const float P = sc.step(e, i, lane);
-            if (i < len) {
-                if constexpr (MODE == kProp) srow[i] = e;
-                if constexpr (MODE == kExact) xh[i] = e;
-                if constexpr (MODE == kFlash) xh[i] = P;
+        if constexpr (MODE == kFlash) {
+            for (int i0 = 0; i0 < len; i0 += 32) {
+                const int i = i0 + lane;
+                const float e = (i < len) ? __expf(xh[i] - m) : 0.f;
+                const float P = sc.step(e, i, lane);
+                if (i < len) xh[i] = P;
             }
+            sc.finish();
+            z = sc.carry;
+        } else {
+            float zl = 0.f;
+            float *srow = nullptr;
+            if constexpr (MODE == kProp) srow = p.stash + size_t(hq0 + h) * p.total_tokens + tok0;
+            for (int i = lane; i < len; i += 32) {
+                const float e = __expf(xh[i] - m);
+                if constexpr (MODE == kProp) srow[i] = e;
+                if constexpr (MODE == kExact) es[i * G + h] = e;
+                zl += e;
+            }
+            z = warp_sum(zl);
         }
-        sc.finish();
-        const float z = sc.carry;
         const size_t rec = (size_t(b) * p.Hq + hq0 + h) * p.Tmax + t;
         if (lane == 0) {
             p.rec_m[rec] = m;
@@ -260,38 +298,44 @@ __global__ void __launch_bounds__(kTileWarps * 32)
 
     // ---- exact: stream the tile's V rows, o_t = sum_i e_i V_i per head
     if constexpr (MODE == kExact) {
-        __syncthreads();  // e of every head is in xs
-        float acc[G][kE];
+        __syncthreads();  // e of every head is in es
+        // this lane's D/32 elements of a row: byte offset lane * kE * kES
+        constexpr int kLaneBytes = kE * Geo::kES;
+        const int jv = (lane * kLaneBytes) >> 4, inner = (lane * kLaneBytes) & 15;
+        float2 acc[G][(kE + 1) / 2];
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int e = 0; e < kE; ++e) acc[h][e] = 0.f;
-        for (int c = nk; c < nchunks; ++c) {
+            for (int q = 0; q < (kE + 1) / 2; ++q) acc[h][q] = make_float2(0.f, 0.f);
+        for (int r = 0; r < nr; ++r) {
+            const int c = nr + r;
             wait_chunk(c);
-            const unsigned char *base = stage + (c % kStages) * Geo::kChunkBytes;
+            const unsigned char *base = wslots + (c % nslot) * Geo::kChunkBytes;
+            const int key_base = r * kRoundKeys + warp * kWarpRows;
+            const int nkeys = min(kWarpRows, len - key_base);
+            for (int kk = 0; kk < nkeys; ++kk) {
+                RowSlice<T, D> row;
+                row.load_shared(base + swz(kk, jv) + inner, 0);
+                const float *eh = es + (key_base + kk) * G;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const int key = warp * 8 + kk;
-                const int kidx = (c - nk) * kChunk + key;
-                if (kidx < len) {
-                    RowSlice<T, D> r;
-                    r.load_shared(base + key * Geo::kRowBytes, lane);
+                for (int h = 0; h < G; ++h) {
+                    const float e = eh[h];
+                    const float2 ee = make_float2(e, e);
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float e = xs[h * tile + kidx];
-#pragma unroll
-                        for (int q = 0; q < kE; ++q) acc[h][q] = fmaf(e, r.v[q], acc[h][q]);
-                    }
+                    for (int q = 0; q < kE / 2; ++q)
+                        acc[h][q] = __ffma2_rn(ee, make_float2(row.v[2 * q], row.v[2 * q + 1]), acc[h][q]);
                 }
             }
-            __syncthreads();
             release_chunk(c);
         }
         float *red = reinterpret_cast<float *>(smem + Lay::red_off(tile));
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int q = 0; q < kE; ++q) red[(warp * G + h) * D + lane * kE + q] = acc[h][q];
+            for (int q = 0; q < kE / 2; ++q) {
+                red[(warp * G + h) * D + lane * kE + 2 * q] = acc[h][q].x;
+                red[(warp * G + h) * D + lane * kE + 2 * q + 1] = acc[h][q].y;
+            }
         __syncthreads();
         for (int idx = tid; idx < G * D; idx += kTileWarps * 32) {
             const int h = idx / D, dd = idx % D;
@@ -304,11 +348,11 @@ __global__ void __launch_bounds__(kTileWarps * 32)
 
     // ---- a timed-out wait: flag it, and let copies still in flight land before exiting
     __syncthreads();
-    if (tid == 0 && s_fail[0]) {
-        raise_flag(p, SANTA_ERR_TIMEOUT);
+    if (lane == 0 && s_fail[0]) {
+        if (warp == 0) raise_flag(p, SANTA_ERR_TIMEOUT);
         const long long t0 = clock64();
-        for (int c = max(0, issued - kStages); c < issued; ++c)
-            while (!mbar_try_wait(&bars[c % kStages], (c / kStages) & 1) && clock64() - t0 < kWaitCycles) {
+        for (int c = max(0, issued - nslot); c < issued; ++c)
+            while (!mbar_try_wait(&wbars[c % nslot], (c / nslot) & 1) && clock64() - t0 < kWaitCycles) {
             }
     }
 }

@@ -36,6 +36,8 @@ def run(inp: Inputs, mode: str, S: int | None = None, U_index: int = 0, debug: b
     res = {"out": out.cpu().numpy()}
     for name, t in bufs.items():
         res[name] = t.cpu().numpy()
+    if "error_flags" in res:  # a bounded wait that gave up, or a flagged input, fails the call
+        assert int(res["error_flags"][0]) == 0, f"device error flags {int(res['error_flags'][0]):#x}"
     res["sample_stride"] = sample_stride
     return res
 

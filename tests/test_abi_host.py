@@ -59,13 +59,14 @@ def _north_star(sd, **kw):
 
 
 def test_workspace_layout_matches_the_byte_model(sd):
-    """prop: 2 tile-record arrays, the fp32 score stash [Hq][n_k], the pass-2
-    partials [B][Hq][ceil(T/16)][d] and one ticket per head, each rounded up to 256 B."""
+    """prop: 2 tile-record arrays [B][Hq][T] and the fp32 score stash [Hq][n_k];
+    flash/exact: the records and the tile estimates [B][Hq][T][d]; each rounded
+    up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _north_star(sd)
     T = 32768 // 256
     rec = r(1 * 32 * T * 4)
-    prop = 2 * rec + r(32 * 32768 * 4) + r(1 * 32 * (T // 16) * 128 * 4) + r(32 * 4)
+    prop = 2 * rec + r(32 * 32768 * 4)
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
     flash = 2 * rec + r(1 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_FLASH) == flash

@@ -48,13 +48,16 @@ def test_static_scratch_matches_the_workspace_entry_point(sd):
                           tile=128, S=64, dtype="bf16", lengths=(5000, 0, 1234), planted_per_head=4, sinks=4)),
     ]
     dev = [to_torch(inp) for inp in cases]
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dbg = sd.Debug()
+    dbg.error_flags = flags.data_ptr()
     outs = []
     for inp, (q, k, v, ind, U) in zip(cases, dev):  # the two static-scratch calls, back to back
         w = inp.workload
         out = torch.full((w.batch, w.num_q_heads, w.head_dim), float("nan"), device="cuda")
-        sd.santa_decode_prop_static_scratch(_problem(sd, inp), q, k, v, ind, U, out)
+        sd.santa_decode_prop_static_scratch(_problem(sd, inp), q, k, v, ind, U, out, debug=dbg)
         outs.append(out)
-    torch.cuda.synchronize()
+    assert sd.santa_read_device_error(flags) == 0
     for inp, (q, k, v, ind, U), got in zip(cases, dev, outs):
         p = _problem(sd, inp)
         ws = torch.empty(sd.workspace_size(p, sd.MODE_PROP), dtype=torch.uint8, device="cuda")
