@@ -205,10 +205,11 @@ class ClockSampler:
 def byte_model(inp, mode: str, S: int, sample_idx=None):
     """Algorithmic HBM bytes of one call and of its dominant kernel.
 
-    prop:  K (Hkv * sum L * d * e) + q + stash write (Hq * sum L * 4) + tile
-           records (written by pass 1, read by pass 2: 2 * 8 * B * Hq * T) +
-           stash read of the tiles that received samples (4 * len per tile) +
-           the distinct V rows the samples touch (d * e each, per KV head) + out.
+    prop:  K (Hkv * sum L * d * e) + q + stash write (Hq * sum L * 4) + the
+           partition records, one (m, z) per 32-key chunk (written by pass 1,
+           read by pass 2: 2 * 8 * Hq * sum ceil(L / 32)) + the stash of the
+           chunks that received samples (4 * len per chunk) + the distinct V
+           rows the samples touch (d * e each, per KV head) + out.
     flash: K + q + distinct V rows + tile partials and records (written and read) + out.
     exact: K + V + q + tile partials and records (written and read) + out.
     Pass 1 / the tile kernel: K + q + its writes.
@@ -217,12 +218,12 @@ def byte_model(inp, mode: str, S: int, sample_idx=None):
     e = 2 if w.dtype == "bf16" else 4
     L = inp.lengths.astype(np.int64)
     T = -(-L // w.tile)
-    sumL, sumT = int(L.sum()), int(T.sum())
+    NC = -(-L // 32)
+    sumL, sumT, sumC = int(L.sum()), int(T.sum()), int(NC.sum())
     B, Hq, Hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
     K = Hkv * sumL * d * e
     q = B * Hq * d * e
     out = B * Hq * d * 4
-    rec = 8 * Hq * sumT  # (m_t, z_t) per (b, h, t)
     vrows = 0
     stash_read = 0
     if sample_idx is not None and mode in ("prop", "flash"):
@@ -234,17 +235,19 @@ def byte_model(inp, mode: str, S: int, sample_idx=None):
                 vrows += rows.size
                 if mode == "prop":
                     for h in range(G):
-                        ts = np.unique(sample_idx[b, g * G + h] // w.tile)
-                        for t in ts:
-                            stash_read += 4 * int(min(w.tile, L[b] - t * w.tile))
+                        for c in np.unique(sample_idx[b, g * G + h] // 32):
+                            stash_read += 4 * int(min(32, L[b] - c * 32))
     if mode == "prop":
+        rec = 8 * Hq * sumC  # (m_c, z_c) per (b, h, chunk)
         main = K + q + Hq * sumL * 4 + rec
         total = main + rec + stash_read + vrows * d * e + out
     elif mode == "flash":
+        rec = 8 * Hq * sumT  # (m_t, z_t) per (b, h, t)
         part = 4 * Hq * sumT * d
         main = K + q + rec + part + vrows * d * e
         total = main + rec + part + out
     else:
+        rec = 8 * Hq * sumT
         part = 4 * Hq * sumT * d
         main = 2 * K + q + rec + part
         total = main + rec + part + out

@@ -6,14 +6,17 @@
  *
  *   santa_decode_prop   S2ANTA-prop: a split-KV pass computes the logits
  *                       x = q.k / sqrt(d) of every key, stashes the
- *                       exponentiated scores and one partition sum Z_tile per
- *                       tile; a reducer forms Z = sum Z_tile and places the S
+ *                       exponentiated scores and one partition sum per block
+ *                       of keys (a 32-key chunk; a tile is tile/32 of them);
+ *                       a reducer forms Z from them and places the S
  *                       systematic thresholds U + m/S on the global CDF, so a
- *                       tile's budget S_tile is the number of thresholds in its
- *                       CDF interval (0 for low-mass tiles, which read no V);
- *                       a second pass searches the stashed in-tile CDF for each
- *                       threshold and averages the chosen V rows:
- *                       out = (1/S) sum_m V[J_m].
+ *                       block's budget is the number of thresholds in its CDF
+ *                       interval (0 for low-mass blocks, which read no V);
+ *                       a second pass searches the stashed in-block CDF for
+ *                       each threshold and averages the chosen V rows:
+ *                       out = (1/S) sum_m V[J_m].  The sample is the one
+ *                       systematic sample of the global CDF, whatever the
+ *                       block size; a tile's S_tile is the sum over its blocks.
  *                       ("Stochastic Sparse Attention for Memory-Bound
  *                       Inference", paper notes, Key designs 1 and 2.)
  *   santa_decode_flash  S2ANTA-flash: every tile draws S_loc = ceil(S / T_b)
@@ -111,7 +114,9 @@ typedef struct {
 typedef struct {
     float *tile_m;           /* [B][Hq][Tmax] max logit of each tile */
     float *tile_z;           /* [B][Hq][Tmax] sum of exp(x - tile_m) over the tile */
-    int *tile_count;         /* [B][Hq][Tmax] prop: S_tile; flash: S_loc of the tile */
+    int *tile_count;         /* [B][Hq][Tmax] prop: S_tile; flash: S_loc of the tile
+                                (prop writes tile_m, tile_z and tile_count in pass 2,
+                                from its 32-key chunk records) */
     int *sample_idx;         /* prop:  [B][Hq][S], key index within the sequence of
                                        sample m (thresholds in increasing order);
                                 flash: [B][Hq][Tmax][sample_stride], the first
@@ -132,9 +137,13 @@ int santa_workspace_size(const santa_problem *p, int mode, size_t *bytes);
 /*
  * S2ANTA-prop decode (paper notes, Key designs 1-2).
  * q, k, v, kv_indptr, U, out, workspace: device pointers as described above.
- * Two kernels on `stream`: pass 1 (scores, stash, tile records) and pass 2
- * (reducer over the T_b tile records, per-tile systematic search, V gather,
- * deterministic combine).  Returns a status; see the conventions above.
+ * Two kernels on `stream`: pass 1 (scores, stash, one record per 32-key chunk)
+ * and pass 2 (reducer over the ceil(L_b / 32) chunk records, per-chunk
+ * systematic search, V gather, deterministic combine).  Workspace: the chunk
+ * records, 2 x [B][Hq][ceil(max_len / 32)] float32, and the score stash
+ * [Hq][total_tokens] float32.  Supported up to max_len of about 4 million keys
+ * (pass 2 keeps its share of the chunk records in shared memory; longer is
+ * SANTA_UNSUPPORTED).  Returns a status; see the conventions above.
  */
 int santa_decode_prop(const santa_problem *p, const void *q, const void *k, const void *v,
                       const long long *kv_indptr, const float *U, float *out,
@@ -181,8 +190,8 @@ int exact_decode(const santa_problem *p, const void *q, const void *k, const voi
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture.  Every call shares the one array, which keeps the last
- * call's contents; what must start at zero is reset inside each call, so results
- * never depend on an earlier call.  Calls whose kernels overlap on the GPU
+ * call's contents; no scratch value has to start at zero (each call writes every
+ * value before reading it), so results never depend on an earlier call.  Calls whose kernels overlap on the GPU
  * (unordered streams or threads) race on the array: order them.
  */
 int santa_decode_prop_static_scratch(const santa_problem *p, const void *q, const void *k, const void *v,

@@ -25,7 +25,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Layout {
-    int Tmax = 0, nsplit = 0, tps = 0;
+    int Tmax = 0, nch = 0, nsplit = 0, cps = 0;
     size_t rec_m = 0, rec_z = 0, stash = 0, partial = 0, total = 0;
 };
 
@@ -49,26 +49,32 @@ int check_problem(const santa_problem *p, int mode) {
 
 // Workspace regions of one call, each 256-byte aligned.  Sizes are computed in
 // double first so that absurd shapes are rejected instead of wrapping around.
+//   prop:        chunk records rec_m, rec_z [B][Hq][nch], nch = ceil(max_len / 32),
+//                and the score stash [Hq][total_tokens];
+//   flash/exact: tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d].
 int make_layout(const santa_problem *p, int mode, Layout *L) {
     const int Tmax = (p->max_len + p->tile - 1) / p->tile;
+    const int nch = (p->max_len + 31) / 32;
+    const bool prop = mode == SANTA_MODE_PROP;
     const double B = p->batch, Hq = p->num_q_heads, D = p->head_dim;
-    const double nrec = B * Hq * Tmax;
+    const double nrec = B * Hq * (prop ? nch : Tmax);
     double est = 2 * nrec * 4;
-    if (mode == SANTA_MODE_PROP)
+    if (prop)
         est += Hq * double(p->total_tokens) * 4;
     else
         est += nrec * D * 4;
     if (est > 1e15) return SANTA_INVALID_ARG;
 
-    const size_t n_rec = size_t(p->batch) * p->num_q_heads * size_t(Tmax);
+    const size_t n_rec = size_t(p->batch) * p->num_q_heads * size_t(prop ? nch : Tmax);
     size_t off = 0;
     L->Tmax = Tmax;
-    prop_split(Tmax, &L->nsplit, &L->tps);
+    L->nch = nch;
+    prop_split(nch, p->tile, &L->nsplit, &L->cps);
     L->rec_m = off;
     off += align256(n_rec * 4);
     L->rec_z = off;
     off += align256(n_rec * 4);
-    if (mode == SANTA_MODE_PROP) {
+    if (prop) {
         L->stash = off;
         off += align256(size_t(p->num_q_heads) * size_t(p->total_tokens) * 4);
     } else {
@@ -80,19 +86,21 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
 }
 
 int smem_check(const santa_problem *p, int mode) {
+    constexpr size_t kOptin = 227 * 1024;  // shared memory a block may opt in to on sm_103
     const int G = p->num_q_heads / p->num_kv_heads;
     size_t need = 0;
-    if (mode == SANTA_MODE_PROP)
-        need = prop_pass1_smem(p->dtype, p->head_dim, G, p->tile);
-    else if (mode == SANTA_MODE_FLASH)
-        need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
-    else
-        need = exact_tile_smem(p->dtype, p->head_dim, G, p->tile);
     if (mode == SANTA_MODE_PROP) {
-        const size_t s2 = prop_pass2_smem(p->head_dim, p->tile, (p->max_len + p->tile - 1) / p->tile);
+        Layout L;
+        if (make_layout(p, mode, &L) != SANTA_OK) return SANTA_INVALID_ARG;
+        need = prop_pass1_smem(p->dtype, p->head_dim, G, int(kOptin));
+        const size_t s2 = prop_pass2_smem(p->head_dim, L.cps);
         if (s2 > need) need = s2;
+    } else if (mode == SANTA_MODE_FLASH) {
+        need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
+    } else {
+        need = exact_tile_smem(p->dtype, p->head_dim, G, p->tile);
     }
-    return need <= 227 * 1024 ? SANTA_OK : SANTA_UNSUPPORTED;
+    return need <= kOptin ? SANTA_OK : SANTA_UNSUPPORTED;
 }
 
 // ---- TMA descriptors of a [total_tokens][Hkv][d] cache: boxes of 128 bytes of one
@@ -194,6 +202,7 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     prm.tile = p->tile;
     prm.S = mode == SANTA_MODE_EXACT ? 1 : p->S;
     prm.Tmax = L.Tmax;
+    prm.nch = L.nch;
     prm.max_len = p->max_len;
     prm.total_tokens = p->total_tokens;
     prm.scale = float(1.0 / std::sqrt(double(p->head_dim)));
@@ -208,7 +217,7 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     prm.stash = mode == SANTA_MODE_PROP ? reinterpret_cast<float *>(ws + L.stash) : nullptr;
     prm.partial = mode == SANTA_MODE_PROP ? nullptr : reinterpret_cast<float *>(ws + L.partial);
     prm.nsplit = L.nsplit;
-    prm.tiles_per_split = L.tps;
+    prm.chunks_per_split = L.cps;
     Timing tm;
     if (dbg) {
         prm.dbg_tile_m = dbg->tile_m;
@@ -222,18 +231,20 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     }
 
     CUtensorMap kmap, vmap;
-    if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows)) return SANTA_CUDA_ERROR;
     cudaError_t e;
     if (mode == SANTA_MODE_PROP) {
-        CUtensorMap kmap32;
-        if (!kv_map(&kmap32, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32)) return SANTA_CUDA_ERROR;
-        e = launch_prop(prm, p->dtype, kmap, kmap32, stream, tm);
-    } else if (mode == SANTA_MODE_FLASH) {
-        e = launch_flash(prm, p->dtype, kmap, stream, tm);
+        if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32)) return SANTA_CUDA_ERROR;
+        e = launch_prop(prm, p->dtype, kmap, stream, tm);
     } else {
-        if (!kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
+        if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
             return SANTA_CUDA_ERROR;
-        e = launch_exact(prm, p->dtype, kmap, vmap, stream, tm);
+        if (mode == SANTA_MODE_FLASH) {
+            e = launch_flash(prm, p->dtype, kmap, stream, tm);
+        } else {
+            if (!kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
+                return SANTA_CUDA_ERROR;
+            e = launch_exact(prm, p->dtype, kmap, vmap, stream, tm);
+        }
     }
     if (e == cudaErrorNotSupported) return SANTA_UNSUPPORTED;
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SANTA_CUDA_ERROR;

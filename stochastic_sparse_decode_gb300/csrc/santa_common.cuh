@@ -15,7 +15,7 @@ namespace santa {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kTileWarps = 4;    // warps of a tile CTA
-constexpr int kWarpRows = 64;    // K/V rows per TMA chunk of one warp (2 per lane)
+constexpr int kWarpRows = 64;    // K/V rows per TMA chunk of one tile-kernel warp (2 per lane)
 constexpr int kPass2Warps = 8;   // warps of a prop pass-2 CTA
 constexpr int kMaxSplit = 8;     // prop pass 2: CTAs per head = size of its cluster
 constexpr int kMergeThreads = 128;
@@ -26,6 +26,7 @@ enum Mode { kProp = 0, kFlash = 1, kExact = 2 };
 // Everything a kernel needs; built by the host entry points.
 struct Params {
     int B, Hq, Hkv, G, D, tile, S, Tmax, max_len;
+    int nch;  // prop: 32-key chunks per sequence slot, ceil(max_len / 32)
     long long total_tokens;
     float scale;  // 1/sqrt(d)
     const void *q, *k, *v;
@@ -33,10 +34,11 @@ struct Params {
     const float *U;
     float *out;
     // workspace
-    float *rec_m, *rec_z;  // [B][Hq][Tmax] tile max logit, tile partition sum
-    float *stash;          // prop: [Hq][total_tokens] exp(x - m_t)
+    float *rec_m, *rec_z;  // flash/exact: [B][Hq][Tmax] tile max logit and partition sum;
+                           // prop: [B][Hq][nch] the same per 32-key chunk
+    float *stash;          // prop: [Hq][total_tokens] exp(x - m_c)
     float *partial;        // flash/exact: [B][Hq][Tmax][D] tile estimates
-    int nsplit, tiles_per_split;  // prop pass 2: CTAs (one cluster) per head, tiles per CTA
+    int nsplit, chunks_per_split;  // prop pass 2: CTAs (one cluster) per head, chunks per CTA
     // optional debug outputs
     float *dbg_tile_m, *dbg_tile_z;
     int *dbg_count, *dbg_idx;
@@ -81,11 +83,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` waiting for the
+// phase (it wakes as soon as the phase completes): waiting warps do not spin
+// through issue slots that working warps on the same scheduler need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Waits for phase `parity` of `bar` to complete; gives up after kWaitCycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 1u << 20)) {
         if (clock64() - t0 > kWaitCycles) return false;
     }
     return true;

@@ -10,15 +10,17 @@
 
 namespace santa {
 
-// prop pass 2: CTAs per head (a cluster of at most kMaxSplit) and tiles per CTA
-// (a multiple of the warp count, at least two per warp).
-inline void prop_split(int Tmax, int *nsplit, int *tps) {
-    int n = (Tmax + 2 * kPass2Warps - 1) / (2 * kPass2Warps);
+// prop pass 2: CTAs per head (a cluster of at most kMaxSplit) and 32-key chunks
+// per CTA -- whole tiles (so a tile's debug totals stay in one CTA) and a
+// multiple of the warp count; about 128 chunks (16 per warp) per CTA.
+inline void prop_split(int nch, int tile, int *nsplit, int *cps) {
+    const int unit = (tile / 32) > kPass2Warps ? tile / 32 : kPass2Warps;
+    int n = (nch + 127) / 128;
     n = n < 1 ? 1 : (n > kMaxSplit ? kMaxSplit : n);
-    int per = (Tmax + n - 1) / n;
-    per = (per + kPass2Warps - 1) / kPass2Warps * kPass2Warps;
+    int per = (nch + n - 1) / n;
+    per = (per + unit - 1) / unit * unit;
     *nsplit = n;
-    *tps = per < kPass2Warps ? kPass2Warps : per;
+    *cps = per < unit ? unit : per;
 }
 
 // Launches `kern` on `stream`; with `pdl` the kernel may start while the
@@ -80,16 +82,15 @@ struct Timing {
 };
 
 // Mode launchers (one translation unit each).  `dtype` is SANTA_F32/SANTA_BF16.
-// kmap64 / kmap32: K descriptors with boxes of 64 rows (tile kernel) and 32 rows (streaming kernel).
-cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap64, const CUtensorMap &kmap32,
-                        cudaStream_t stream, const Timing &tm);
+// kmap32: the K descriptor with boxes of 32 rows (the streaming pass-1 kernel).
+cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm);
 cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
 cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          cudaStream_t stream, const Timing &tm);
 
 // Shared-memory needs, for validation on the host.
-size_t prop_pass1_smem(int dtype, int D, int G, int tile);
-size_t prop_pass2_smem(int D, int tile, int Tmax);
+size_t prop_pass1_smem(int dtype, int D, int G, int smem_optin);
+size_t prop_pass2_smem(int D, int cps);
 size_t flash_tile_smem(int dtype, int D, int G, int tile);
 size_t exact_tile_smem(int dtype, int D, int G, int tile);
 

@@ -2,28 +2,32 @@
 // flash / exact merge.
 //
 // prop pass 2 ("Stochastic Sparse Attention for Memory-Bound Inference", paper
-// notes, Key design 2).  The tiles of one (query head, sequence) are split over
-// the CTAs of one thread-block cluster (`nsplit` CTAs, `tiles_per_split` tiles
-// each, two or more per warp).  Every CTA first runs the reducer over that
-// head's T_b tile records, in a fixed order, so all of them obtain
-// bit-identical values:
-//     M = max_t m_t,   w_t = z_t exp(m_t - M)   (Z_tile on a common scale),
-//     C_t = w_0 + ... + w_t (inclusive),   Z = C_{T_b - 1}.
+// notes, Key design 2), on the 32-key chunk records of pass 1.  The chunks of
+// one (query head, sequence) are split over the CTAs of one thread-block
+// cluster (`nsplit` CTAs of `chunks_per_split` chunks, whole tiles and whole
+// warps each).  Every CTA first runs the reducer over all of that head's
+// chunk records, in a fixed order, so all of them obtain bit-identical values:
+//     M = max_c m_c,   w_c = z_c exp(m_c - M)   (the chunks' mass on one scale),
+//     C_c = w_0 + ... + w_c (inclusive),   Z = C_{N_b - 1}.
 // The systematic thresholds are U + m/S, m = 0..S-1 (Key design 1), i.e. the
 // points (U + m/S) Z on the unnormalised CDF.  The number of them below c is
 //     N(c) = clamp(ceil(S c / Z - S U), 0, S),
-// so tile t receives the thresholds m in [N(C_{t-1}), N(C_t)) -- its budget
-// S_tile = N(C_t) - N(C_{t-1}), with N(C_{-1}) = 0 and N(C_{T_b - 1}) = S.
-// N is evaluated by monotone float operations on non-decreasing C, so budgets
-// are non-negative and add up to exactly S.  Tiles with S_tile = 0 read
-// neither their stash nor V.  For the others one warp scans the tile's stashed
-// e into its in-tile prefix, maps each threshold to the tile's own scale,
-//     r_m = ((U + m/S) Z - C_{t-1}) / exp(m_t - M),
-// takes the smallest key whose prefix exceeds r_m (clamped to the tile's keys
-// of positive score), and adds V of that key.  Each CTA sums its warps in warp
-// order and stores the sum into the shared memory of cluster rank 0, which adds
-// the CTAs in rank order after one cluster barrier.  out = sum / S: no multiply
-// by a probability anywhere after the softmax.
+// so chunk c receives the thresholds m in [N(C_{c-1}), N(C_c)), with
+// N(C_{-1}) = 0 and N(C_{N_b - 1}) = S.  The scan is taken as a running
+// maximum as well, so C is non-decreasing whatever the order of the float
+// additions, budgets are never negative and add up to exactly S.  Chunks with
+// no threshold read neither their stash nor V (a warp's first 16 chunks are
+// read speculatively, in the round trip of the records).  For the others the
+// warp scans the chunk's 32 stashed e into its in-chunk prefix, maps each
+// threshold to the chunk's own scale,
+//     r_m = ((U + m/S) Z - C_{c-1}) / exp(m_c - M),
+// takes the smallest key whose prefix exceeds r_m (clamped to the chunk's keys
+// of positive score), and queues that key; the queue is flushed by gathering
+// up to 32 V rows at a time.  Each CTA sums its warps in warp order and stores
+// the sum into the shared memory of cluster rank 0, which adds the CTAs in
+// rank order after one cluster barrier.  out = sum / S: no multiply by a
+// probability anywhere after the softmax.  A tile's budget S_tile (a debug
+// output, with its Z_tile and m_t) is the sum over its chunks.
 //
 // merge (flash, Key design 3; exact split-KV): per (query head, sequence)
 //     flash: out = sum_t w_t o_t / Z   with o_t the tile's sample average,
@@ -32,6 +36,7 @@
 #pragma once
 
 #include "santa_common.cuh"
+#include "santa_stream.cuh"
 #include "santa_tile.cuh"
 
 namespace santa {
@@ -83,46 +88,64 @@ __device__ __forceinline__ float block_inclusive_scan(float v, float *scr, float
     return v + off;
 }
 
-// Pass-2 shared memory: [tps+1] C, [tps] first, [tps] count, [8] scratch,
-// [Tmax] tile max, [Tmax] tile sum, [NW][2][tile] in-tile prefixes, [NW][D]
-// warp sums, [8][D] the cluster's CTA sums (used in rank 0).
+// Inclusive scan (op = max) over the block; every thread gets its prefix.
+template <int NW>
+__device__ __forceinline__ float block_inclusive_max(float v, float *scr) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v = fmaxf(v, u);
+    }
+    __syncthreads();
+    if (lane == 31) scr[warp] = v;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+        if (w < warp) v = fmaxf(v, scr[w]);
+    return v;
+}
+
+constexpr int kP2Rec = 4;     // chunk records per thread per reducer block
+constexpr int kP2Batch = 16;  // chunks of a warp whose stash is read in one batch
+
+// Pass-2 shared memory (prop): [cps+1] C (running max, from C_{c_lo-1}),
+// [cps+1] threshold counts N, [cps] exp(m_c - M), [64] scratch, per warp
+// [16][32] stash batch, [32] in-chunk prefix, [32] queued keys and [D] sum,
+// [8][D] the cluster's CTA sums (used in rank 0).
 template <typename T, int D>
 struct Pass2Smem {
-    static __host__ __device__ size_t rec_off(int tps) { return (size_t(tps + 1) * 4 + size_t(tps) * 8 + 32 + 15) & ~size_t(15); }
-    static __host__ __device__ size_t buf_off(int tps, int Tmax) {
-        return (rec_off(tps) + size_t(Tmax) * 8 + 15) & ~size_t(15);
-    }
-    static __host__ __device__ size_t red_off(int tps, int Tmax, int tile) {
-        return buf_off(tps, Tmax) + size_t(kPass2Warps) * 2 * tile * 4;
-    }
-    static __host__ __device__ size_t part_off(int tps, int Tmax, int tile) {
-        return red_off(tps, Tmax, tile) + size_t(kPass2Warps) * D * 4;
-    }
-    static __host__ __device__ size_t bytes(int tps, int Tmax, int tile) {
-        return part_off(tps, Tmax, tile) + size_t(kMaxSplit) * D * 4;
-    }
+    static __host__ __device__ size_t n_off(int cps) { return size_t(cps + 1) * 4; }
+    static __host__ __device__ size_t st_off(int cps) { return n_off(cps) + size_t(cps + 1) * 4; }
+    static __host__ __device__ size_t scr_off(int cps) { return (st_off(cps) + size_t(cps) * 4 + 15) & ~size_t(15); }
+    static __host__ __device__ size_t ev_off(int cps) { return scr_off(cps) + 64 * 4; }
+    static __host__ __device__ size_t wb_off(int cps) { return ev_off(cps) + size_t(kPass2Warps) * kP2Batch * 32 * 4; }
+    static __host__ __device__ size_t wl_off(int cps) { return wb_off(cps) + size_t(kPass2Warps) * 32 * 4; }
+    static __host__ __device__ size_t red_off(int cps) { return wl_off(cps) + size_t(kPass2Warps) * 32 * 4; }
+    static __host__ __device__ size_t part_off(int cps) { return red_off(cps) + size_t(kPass2Warps) * D * 4; }
+    static __host__ __device__ size_t bytes(int cps) { return part_off(cps) + size_t(kMaxSplit) * D * 4; }
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const Params p) {
+__global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Params p) {
     constexpr int kThreads = kPass2Warps * 32;
     constexpr int kE = D / 32;
-    constexpr int kPre = 8;  // stash values per lane and tile read in one batch (first 256 keys)
+    constexpr int kBlk = kThreads * kP2Rec;
     using Lay = Pass2Smem<T, D>;
     const int split = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;  // split == rank in the cluster
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = p.tile, tps = p.tiles_per_split, kpw = tps / kPass2Warps;
+    const int cps = p.chunks_per_split, kper = cps / kPass2Warps;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    float *sC = reinterpret_cast<float *>(smem);  // C_{t_lo-1} .. C_{t_hi-1}
-    int *s_first = reinterpret_cast<int *>(sC + tps + 1);
-    int *s_cnt = s_first + tps;
-    float *scr = reinterpret_cast<float *>(s_cnt + tps);  // [8]
-    float *s_m = reinterpret_cast<float *>(smem + Lay::rec_off(tps));
-    float *s_z = s_m + p.Tmax;
-    float *buf = reinterpret_cast<float *>(smem + Lay::buf_off(tps, p.Tmax));
-    float *red = reinterpret_cast<float *>(smem + Lay::red_off(tps, p.Tmax, tile));
-    float *part = reinterpret_cast<float *>(smem + Lay::part_off(tps, p.Tmax, tile));
+    float *sC = reinterpret_cast<float *>(smem);                   // C of chunks c_lo-1 .. c_hi-1
+    int *sN = reinterpret_cast<int *>(smem + Lay::n_off(cps));     // N of the same
+    float *s_st = reinterpret_cast<float *>(smem + Lay::st_off(cps));
+    float *scr = reinterpret_cast<float *>(smem + Lay::scr_off(cps));
+    float *wev = reinterpret_cast<float *>(smem + Lay::ev_off(cps)) + warp * kP2Batch * 32;
+    float *wb = reinterpret_cast<float *>(smem + Lay::wb_off(cps)) + warp * 32;
+    int *wl = reinterpret_cast<int *>(smem + Lay::wl_off(cps)) + warp * 32;
+    float *red = reinterpret_cast<float *>(smem + Lay::red_off(cps));
+    float *part = reinterpret_cast<float *>(smem + Lay::part_off(cps));
 
     cluster_arrive();  // first half of the barrier that makes every CTA's shared memory addressable
 
@@ -132,149 +155,176 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     const float u = load_offset(p, b, hq);
     pdl_wait();
 
-    const int Tb = (L + tile - 1) / tile;
-    const int t_lo = split * tps, t_hi = min(Tb, t_lo + tps);
-    const bool active = t_lo < t_hi;  // CTA-uniform: this CTA owns at least one tile
-    const size_t rec0 = (size_t(b) * p.Hq + hq) * p.Tmax;
+    const int Nb = (L + kChunkRows - 1) / kChunkRows;
+    const int c_lo = split * cps, c_hi = min(Nb, c_lo + cps);
+    const bool active = c_lo < c_hi;  // CTA-uniform: this CTA owns at least one chunk
+    const int cw0 = c_lo + warp * kper, cw1 = min(c_hi, cw0 + kper);  // this warp's chunks
+    const size_t rec0 = (size_t(b) * p.Hq + hq) * p.nch;
     const float *sseq = p.stash + size_t(hq) * p.total_tokens + start;
     const float Sf = float(p.S);
-
-    // Stash values of two of this warp's tiles (split-local indices i0, i0 + 8), one batch of loads.
-    auto load_pair = [&](int i0, float (&ev)[2][kPre]) {
-#pragma unroll
-        for (int w2 = 0; w2 < 2; ++w2) {
-            const int t = t_lo + i0 + kPass2Warps * w2;
-            const int lent = (i0 + kPass2Warps * w2 < kpw * kPass2Warps && t < t_hi) ? min(tile, L - t * tile) : 0;
-#pragma unroll
-            for (int k = 0; k < kPre; ++k) {
-                const int idx = lane + 32 * k;
-                ev[w2][k] = idx < lent ? __ldcg(sseq + size_t(t) * tile + idx) : 0.f;
-            }
-        }
-    };
 
     float acc[kE];
 #pragma unroll
     for (int e = 0; e < kE; ++e) acc[e] = 0.f;
 
     if (active) {
-        // ---- one round trip: the first pair of this warp's tiles (speculatively) and all tile records
-        float ev[2][kPre];
-        load_pair(warp, ev);
-        for (int t0 = 0; t0 < Tb; t0 += 4 * kThreads) {
-            float mm[4], zz[4];
+        // ---- one round trip: the first block of chunk records and, speculatively,
+        // the stash of this warp's first batch of chunks
+        float mr[kP2Rec], zr[kP2Rec];
+        auto load_block = [&](int base) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = t0 + k * kThreads + tid;
-                mm[k] = t < Tb ? __ldcg(p.rec_m + rec0 + t) : 0.f;
-                zz[k] = t < Tb ? __ldcg(p.rec_z + rec0 + t) : 0.f;
+            for (int k = 0; k < kP2Rec; ++k) {
+                const int c = base + tid * kP2Rec + k;
+                mr[k] = c < Nb ? __ldcg(p.rec_m + rec0 + c) : -INFINITY;
+                zr[k] = c < Nb ? __ldcg(p.rec_z + rec0 + c) : 0.f;
+            }
+        };
+        load_block(0);
+        {
+            float ev[kP2Batch];
+#pragma unroll
+            for (int k = 0; k < kP2Batch; ++k) {
+                const int c = cw0 + k;
+                const int key = c * kChunkRows + lane;
+                ev[k] = (c < cw1 && key < L) ? __ldcg(sseq + key) : 0.f;
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = t0 + k * kThreads + tid;
-                if (t < Tb) {
-                    s_m[t] = mm[k];
-                    s_z[t] = zz[k];
-                }
-            }
+            for (int k = 0; k < kP2Batch; ++k) wev[k * 32 + lane] = ev[k];
         }
-        __syncthreads();
 
-        // ---- reducer
-        float mx = -INFINITY;
-        for (int t = tid; t < Tb; t += kThreads) mx = fmaxf(mx, s_m[t]);
+        // ---- reducer: M, then the scan (as a running maximum) and the threshold counts
+        float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+        for (int base = kBlk; base < Nb; base += kBlk)
+            for (int k = 0; k < kP2Rec; ++k) {
+                const int c = base + tid * kP2Rec + k;
+                if (c < Nb) mx = fmaxf(mx, __ldcg(p.rec_m + rec0 + c));
+            }
         const float M = block_max<kPass2Warps>(mx, scr);
-        float carry = 0.f;
-        for (int c0 = 0; c0 < Tb; c0 += kThreads) {
-            const int t = c0 + tid;
-            const float w = (t < Tb) ? s_z[t] * expf(s_m[t] - M) : 0.f;
+        float carry = 0.f, carry_max = 0.f;
+        for (int base = 0; base < Nb; base += kBlk) {
+            if (base > 0) load_block(base);
+            float cl[kP2Rec];  // this thread's chunks: local inclusive prefix
+            float run = 0.f;
+#pragma unroll
+            for (int k = 0; k < kP2Rec; ++k) {
+                const float st = expf(mr[k] - M);
+                const int c = base + tid * kP2Rec + k;
+                if (c >= c_lo && c < c_hi) s_st[c - c_lo] = st;
+                run += base + tid * kP2Rec + k < Nb ? zr[k] * st : 0.f;
+                cl[k] = run;
+            }
             float total;
-            const float incl = block_inclusive_scan<kPass2Warps>(w, scr, &total) + carry;
-            if (t >= t_lo - 1 && t < t_hi) sC[t - t_lo + 1] = incl;
-            carry = total + carry;
+            const float incl = block_inclusive_scan<kPass2Warps>(run, scr + 8, &total);
+            const float excl = carry + (incl - run);  // start of this thread's chunks (rounded)
+            float hi = carry_max;
+#pragma unroll
+            for (int k = 0; k < kP2Rec; ++k) hi = fmaxf(hi, excl + cl[k]);
+            const float pre = block_inclusive_max<kPass2Warps>(hi, scr + 16);  // running max up to this thread
+            __syncthreads();
+            if (tid == kThreads - 1) scr[32] = pre;
+            // the running max entering this thread: the previous thread's (for lane 0,
+            // the earlier warps' maxima), and the carry from the earlier blocks
+            float before = __shfl_up_sync(kFull, pre, 1);
+            if (lane == 0) {
+                before = carry_max;
+                for (int w = 0; w < warp; ++w) before = fmaxf(before, scr[16 + w]);
+            }
+            before = fmaxf(before, carry_max);
+#pragma unroll
+            for (int k = 0; k < kP2Rec; ++k) {
+                before = fmaxf(before, excl + cl[k]);
+                const int c = base + tid * kP2Rec + k;
+                if (c >= c_lo - 1 && c < c_hi) sC[c - c_lo + 1] = before;
+            }
+            __syncthreads();
+            carry = carry + total;
+            carry_max = scr[32];
         }
-        const float Z = carry;
-        if (t_lo == 0 && tid == 0) sC[0] = 0.f;
+        const float Z = carry_max;  // = C_{N_b - 1}
+        if (c_lo == 0 && tid == 0) sC[0] = 0.f;
         __syncthreads();
 
         const float SU = Sf * u;
-        auto N = [&](float c) -> int {
-            const float x = ceilf(fmaf(Sf, c / Z, -SU));
-            return int(fminf(fmaxf(x, 0.f), Sf));
-        };
-        for (int i = tid; i < t_hi - t_lo; i += kThreads) {
-            const int t = t_lo + i;
-            const int n_prev = (t == 0) ? 0 : N(sC[i]);
-            const int n_cur = (t == Tb - 1) ? p.S : N(sC[i + 1]);
-            s_first[i] = n_prev;
-            s_cnt[i] = n_cur - n_prev;
-            if (p.dbg_count) p.dbg_count[rec0 + t] = n_cur - n_prev;
+        for (int i = tid; i <= c_hi - c_lo; i += kThreads) {  // N(C_{c-1}) for c = c_lo .. c_hi
+            const int c = c_lo + i - 1;
+            int n;
+            if (c < 0)
+                n = 0;
+            else if (c == Nb - 1)
+                n = p.S;
+            else
+                n = int(fminf(fmaxf(ceilf(fmaf(Sf, sC[i] / Z, -SU)), 0.f), Sf));
+            sN[i] = n;
         }
         __syncthreads();
 
-        // ---- this warp's tiles, two at a time: in-tile prefix, systematic search, V gather
-        float *wb = buf + size_t(warp) * 2 * tile;
+        // ---- debug: per tile of this CTA, m_t, Z_tile (on the m_t scale) and S_tile
+        if (p.dbg_tile_m || p.dbg_tile_z || p.dbg_count) {
+            const int cpt = p.tile / kChunkRows;
+            for (int t = c_lo / cpt + tid; t * cpt < c_hi; t += kThreads) {
+                const int ca = t * cpt, cb = min(c_hi, ca + cpt);
+                float tm = -INFINITY, tz = 0.f;
+                for (int c = ca; c < cb; ++c) tm = fmaxf(tm, __ldcg(p.rec_m + rec0 + c));
+                for (int c = ca; c < cb; ++c) tz += __ldcg(p.rec_z + rec0 + c) * expf(__ldcg(p.rec_m + rec0 + c) - tm);
+                const size_t rt = (size_t(b) * p.Hq + hq) * p.Tmax + t;
+                if (p.dbg_tile_m) p.dbg_tile_m[rt] = tm;
+                if (p.dbg_tile_z) p.dbg_tile_z[rt] = tz;
+                if (p.dbg_count) p.dbg_count[rt] = sN[cb - c_lo] - sN[ca - c_lo];
+            }
+        }
+
+        // ---- this warp's chunks with thresholds: in-chunk prefix, systematic search, queued V gather
         const int kvh = hq / p.G;
         const size_t vstride = size_t(p.Hkv) * D;
         const T *vseq = static_cast<const T *>(p.v) + size_t(start) * vstride + size_t(kvh) * D;
-        for (int kk = 0; kk < kpw; kk += 2) {
-            const int i0 = warp + kPass2Warps * kk;
-            if (kk > 0) load_pair(i0, ev);
-            int cnt[2], first[2], k0[2], len[2], lastp[2];
-            float st[2], Cprev[2];
+        int nq = 0;  // keys queued in wl
+        auto flush = [&]() {
+            __syncwarp();
+            const int j = wl[lane];
+            gather_rows<T, D>(acc, vseq, vstride, j, nq, lane);
+            nq = 0;
+            __syncwarp();
+        };
+        for (int c0 = cw0; c0 < cw1; c0 += kP2Batch) {
+            if (c0 > cw0) {  // later batches: only the chunks that hold a threshold
 #pragma unroll
-            for (int w2 = 0; w2 < 2; ++w2) {
-                const int i = i0 + kPass2Warps * w2;
-                const int t = t_lo + i;
-                const bool mine = (kk + w2 < kpw) && t < t_hi;
-                cnt[w2] = mine ? s_cnt[i] : 0;
-                first[w2] = mine ? s_first[i] : 0;
-                k0[w2] = t * tile;
-                len[w2] = mine ? min(tile, L - t * tile) : 0;
-                lastp[w2] = -1;
-                st[w2] = 1.f;
-                Cprev[w2] = 0.f;
-                if (cnt[w2] > 0) {
-                    TileScan sc;
-                    float *P = wb + w2 * tile;
-#pragma unroll
-                    for (int k = 0; k < kPre; ++k) {
-                        const int idx = lane + 32 * k;
-                        if (32 * k < len[w2]) {
-                            const float v = sc.step(ev[w2][k], idx, lane);
-                            if (idx < len[w2]) P[idx] = v;
-                        }
-                    }
-                    for (int j0 = 32 * kPre; j0 < len[w2]; j0 += 32) {  // tiles longer than 256 keys
-                        const int idx = j0 + lane;
-                        const float e = idx < len[w2] ? __ldcg(sseq + k0[w2] + idx) : 0.f;
-                        const float v = sc.step(e, idx, lane);
-                        if (idx < len[w2]) P[idx] = v;
-                    }
-                    sc.finish();
-                    lastp[w2] = sc.last_pos;
-                    st[w2] = expf(s_m[t] - M);
-                    Cprev[w2] = sC[i];
+                for (int k = 0; k < kP2Batch; ++k) {
+                    const int c = c0 + k;
+                    const int key = c * kChunkRows + lane;
+                    const bool need = c < cw1 && sN[c - c_lo + 1] > sN[c - c_lo];
+                    wev[k * 32 + lane] = (need && key < L) ? __ldcg(sseq + key) : 0.f;
                 }
             }
             __syncwarp();
-            const int total = cnt[0] + cnt[1];
-            for (int g0 = 0; g0 < total; g0 += 32) {
-                const int g = g0 + lane;
-                int j = 0;
-                if (g < total) {
-                    const bool second = g >= cnt[0];  // which of the two tiles holds sample g
-                    const int m = second ? first[1] + (g - cnt[0]) : first[0] + g;
-                    const float thr = u + float(m) / Sf;
-                    const float r = (thr * Z - (second ? Cprev[1] : Cprev[0])) / (second ? st[1] : st[0]);
-                    j = (second ? k0[1] : k0[0]) + cdf_search(wb + (second ? tile : 0), second ? len[1] : len[0], r,
-                                                              second ? lastp[1] : lastp[0]);
-                    if (p.dbg_idx) p.dbg_idx[(size_t(b) * p.Hq + hq) * p.S + m] = j;
+            const int kend = min(kP2Batch, cw1 - c0);
+            for (int k = 0; k < kend; ++k) {
+                const int c = c0 + k, i = c - c_lo;
+                const int first = sN[i], cnt = sN[i + 1] - first;
+                if (cnt <= 0) continue;
+                const float e = wev[k * 32 + lane];
+                wb[lane] = warp_inclusive_scan(e, lane);
+                const unsigned pos = __ballot_sync(kFull, e > 0.f);
+                const int last_pos = pos ? 31 - __clz(pos) : -1;
+                const int len = min(kChunkRows, L - c * kChunkRows);
+                const float Cprev = sC[i], st = s_st[i];
+                __syncwarp();
+                for (int g0 = 0; g0 < cnt; g0 += 32) {
+                    const int nn = min(32, cnt - g0);
+                    if (nq + nn > 32) flush();
+                    if (lane < nn) {
+                        const int m = first + g0 + lane;
+                        const float thr = u + float(m) / Sf;
+                        const float r = (thr * Z - Cprev) / st;
+                        const int j = c * kChunkRows + cdf_search(wb, len, r, last_pos);
+                        wl[nq + lane] = j;
+                        if (p.dbg_idx) p.dbg_idx[(size_t(b) * p.Hq + hq) * p.S + m] = j;
+                    }
+                    nq += nn;
                 }
-                gather_rows<T, D>(acc, vseq, vstride, j, min(32, total - g0), lane);
+                __syncwarp();
             }
-            __syncwarp();
         }
+        if (nq > 0) flush();
     }
 
     // ---- deterministic combine: warps in order, then the cluster's CTAs in rank order

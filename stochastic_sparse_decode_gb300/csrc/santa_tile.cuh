@@ -19,8 +19,6 @@
 // the m_t scale ("Stochastic Sparse Attention for Memory-Bound Inference", paper
 // notes, Key design 2: exponentiated scores plus one Z_tile per tile).  Then:
 //
-//   kProp   writes e to the score stash and (m_t, z_t) to the tile records;
-//           the reducer and the sampling happen in pass 2.
 //   kFlash  samples S_loc = ceil(S / T_b) systematic thresholds U_t + s/S_loc,
 //           U_t = U S / S_loc, on the tile's own CDF (its prefix of e divided
 //           by z_t), gather-averages the chosen V rows into the tile estimate
@@ -253,12 +251,9 @@ __global__ void __launch_bounds__(kTileWarps * 32)
             z = sc.carry;
         } else {
             float zl = 0.f;
-            float *srow = nullptr;
-            if constexpr (MODE == kProp) srow = p.stash + size_t(hq0 + h) * p.total_tokens + tok0;
             for (int i = lane; i < len; i += 32) {
                 const float e = __expf(xh[i] - m);
-                if constexpr (MODE == kProp) srow[i] = e;
-                if constexpr (MODE == kExact) es[i * G + h] = e;
+                es[i * G + h] = e;
                 zl += e;
             }
             z = warp_sum(zl);

@@ -59,22 +59,31 @@ def _north_star(sd, **kw):
 
 
 def test_workspace_layout_matches_the_byte_model(sd):
-    """prop: 2 tile-record arrays [B][Hq][T] and the fp32 score stash [Hq][n_k];
-    flash/exact: the records and the tile estimates [B][Hq][T][d]; each rounded
-    up to 256 B."""
+    """prop: 2 chunk-record arrays [B][Hq][ceil(max_len/32)] and the fp32 score
+    stash [Hq][n_k]; flash/exact: 2 tile-record arrays [B][Hq][T] and the tile
+    estimates [B][Hq][T][d]; each rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _north_star(sd)
-    T = 32768 // 256
-    rec = r(1 * 32 * T * 4)
-    prop = 2 * rec + r(32 * 32768 * 4)
+    T, nch = 32768 // 256, 32768 // 32
+    prop = 2 * r(1 * 32 * nch * 4) + r(32 * 32768 * 4)
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
-    flash = 2 * rec + r(1 * 32 * T * 128 * 4)
+    flash = 2 * r(1 * 32 * T * 4) + r(1 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_FLASH) == flash
     assert sd.workspace_size(p, sd.MODE_EXACT) == flash
-    # ragged tail: T = ceil(max_len / tile)
+    # ragged tail: T = ceil(max_len / tile), chunks = ceil(max_len / 32)
     p = _north_star(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
-    T = 8
+    T, nch = 8, 32
     assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
+    assert sd.workspace_size(p, sd.MODE_PROP) == 2 * r(3 * 32 * nch * 4) + r(32 * 2000 * 4)
+
+
+def test_very_long_prop_contexts_are_unsupported_not_wrong(sd):
+    """Pass 2 keeps a CTA's share of the chunk records in shared memory: a max_len
+    past that is refused on the host (flash and exact still take it)."""
+    p = _north_star(sd, max_len=32 * 1024 * 1024, total_tokens=32 * 1024 * 1024, tile=1024)
+    n = ctypes.c_size_t(0)
+    assert sd.lib().santa_workspace_size(ctypes.byref(p), sd.MODE_PROP, ctypes.byref(n)) == sd.OK
+    assert _call_prop(sd, p) == sd.UNSUPPORTED
 
 
 @pytest.mark.parametrize("field,value,status", [
