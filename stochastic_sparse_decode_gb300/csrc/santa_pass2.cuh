@@ -13,13 +13,14 @@
 // points (U + m/S) Z on the unnormalised CDF.  The number of them below c is
 //     N(c) = clamp(ceil(S c / Z - S U), 0, S),
 // so chunk c receives the thresholds m in [N(C_{c-1}), N(C_c)), with
-// N(C_{-1}) = 0 and N(C_{N_b - 1}) = S.  The scan is taken as a running
-// maximum as well, so C is non-decreasing whatever the order of the float
-// additions, budgets are never negative and add up to exactly S.  Chunks with
-// no threshold read neither their stash nor V (a warp's first 16 chunks are
-// read speculatively, in the round trip of the records).  For the others the
-// warp scans the chunk's 32 stashed e into its in-chunk prefix, maps each
-// threshold to the chunk's own scale,
+// N(C_{-1}) = 0 and N(C_{N_b - 1}) = S.  The masses w_c are summed as 64-bit
+// fixed-point integers, so C is exact whatever the order of the additions:
+// non-decreasing, identical in every CTA, budgets never negative and adding up
+// to exactly S.  Chunks with no threshold read neither their stash nor V (a
+// warp's first 16 chunks are read speculatively, in the round trip of the
+// records).  A warp takes its chunks 16 at a time: it scans the 32 stashed e
+// of each into its in-chunk prefix, then gives every lane one threshold of the
+// batch, maps it to its chunk's own scale,
 //     r_m = ((U + m/S) Z - C_{c-1}) / exp(m_c - M),
 // takes the smallest key whose prefix exceeds r_m (clamped to the chunk's keys
 // of positive score), and queues that key; the queue is flushed by gathering
@@ -88,66 +89,78 @@ __device__ __forceinline__ float block_inclusive_scan(float v, float *scr, float
     return v + off;
 }
 
-// Inclusive scan (op = max) over the block; every thread gets its prefix.
-template <int NW>
-__device__ __forceinline__ float block_inclusive_max(float v, float *scr) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Inclusive prefix sum of 64-bit integers across the warp (exact, so any order of
+// additions gives the same, non-decreasing result).
+__device__ __forceinline__ unsigned long long warp_inclusive_scan_u64(unsigned long long v, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(kFull, v, o);
-        if (lane >= o) v = fmaxf(v, u);
+        const unsigned long long u = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += u;
     }
-    __syncthreads();
-    if (lane == 31) scr[warp] = v;
-    __syncthreads();
+    return v;
+}
+__device__ __forceinline__ int warp_inclusive_scan_int(int v, int lane) {
 #pragma unroll
-    for (int w = 0; w < NW; ++w)
-        if (w < warp) v = fmaxf(v, scr[w]);
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += u;
+    }
     return v;
 }
 
 constexpr int kP2Rec = 4;     // chunk records per thread per reducer block
-constexpr int kP2Batch = 16;  // chunks of a warp whose stash is read in one batch
+constexpr int kP2Batch = 16;  // chunks of a warp taken together (stash read, prefixes, searches)
+// The reducer's partition masses are summed as integers: w * 2^40 rounded.  The
+// largest chunk mass is <= 32 (a chunk's maximum key has e = 1 at the global
+// maximum), and pass 2 accepts at most 2^17 chunks per sequence, so a sum stays
+// below 2^62; the absolute error, <= 2^-41 per chunk, is below 2^-24 of Z >= 1.
+constexpr float kMassScale = 1099511627776.0f;  // 2^40
 
-// Pass-2 shared memory (prop): [cps+1] C (running max, from C_{c_lo-1}),
-// [cps+1] threshold counts N, [cps] exp(m_c - M), [64] scratch, per warp
-// [16][32] stash batch, [32] in-chunk prefix, [32] queued keys and [D] sum,
+// Pass-2 shared memory (prop): [cps+1] C (fixed point, C_{c_lo-1} .. C_{c_hi-1}),
+// [cps+1] threshold counts N of the same, [cps] exp(m_c - M), [48] 64-bit
+// scratch, per warp [16][32] stash batch / in-chunk prefixes, [16] cumulative
+// sample counts, [16] last positive key, [32] queued keys, [8][D] warp sums,
 // [8][D] the cluster's CTA sums (used in rank 0).
 template <typename T, int D>
 struct Pass2Smem {
-    static __host__ __device__ size_t n_off(int cps) { return size_t(cps + 1) * 4; }
+    static __host__ __device__ size_t n_off(int cps) { return size_t(cps + 1) * 8; }
     static __host__ __device__ size_t st_off(int cps) { return n_off(cps) + size_t(cps + 1) * 4; }
     static __host__ __device__ size_t scr_off(int cps) { return (st_off(cps) + size_t(cps) * 4 + 15) & ~size_t(15); }
-    static __host__ __device__ size_t ev_off(int cps) { return scr_off(cps) + 64 * 4; }
-    static __host__ __device__ size_t wb_off(int cps) { return ev_off(cps) + size_t(kPass2Warps) * kP2Batch * 32 * 4; }
-    static __host__ __device__ size_t wl_off(int cps) { return wb_off(cps) + size_t(kPass2Warps) * 32 * 4; }
+    static __host__ __device__ size_t ev_off(int cps) { return scr_off(cps) + 48 * 8; }
+    static __host__ __device__ size_t cum_off(int cps) { return ev_off(cps) + size_t(kPass2Warps) * kP2Batch * 32 * 4; }
+    static __host__ __device__ size_t last_off(int cps) { return cum_off(cps) + size_t(kPass2Warps) * kP2Batch * 4; }
+    static __host__ __device__ size_t wl_off(int cps) { return last_off(cps) + size_t(kPass2Warps) * kP2Batch * 4; }
     static __host__ __device__ size_t red_off(int cps) { return wl_off(cps) + size_t(kPass2Warps) * 32 * 4; }
     static __host__ __device__ size_t part_off(int cps) { return red_off(cps) + size_t(kPass2Warps) * D * 4; }
     static __host__ __device__ size_t bytes(int cps) { return part_off(cps) + size_t(kMaxSplit) * D * 4; }
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Params p) {
+__global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const Params p) {
     constexpr int kThreads = kPass2Warps * 32;
     constexpr int kE = D / 32;
     constexpr int kBlk = kThreads * kP2Rec;
     using Lay = Pass2Smem<T, D>;
+    using u64 = unsigned long long;
     const int split = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;  // split == rank in the cluster
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cps = p.chunks_per_split, kper = cps / kPass2Warps;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    float *sC = reinterpret_cast<float *>(smem);                   // C of chunks c_lo-1 .. c_hi-1
-    int *sN = reinterpret_cast<int *>(smem + Lay::n_off(cps));     // N of the same
+    u64 *sC = reinterpret_cast<u64 *>(smem);                        // C of chunks c_lo-1 .. c_hi-1
+    int *sN = reinterpret_cast<int *>(smem + Lay::n_off(cps));       // N of the same
     float *s_st = reinterpret_cast<float *>(smem + Lay::st_off(cps));
-    float *scr = reinterpret_cast<float *>(smem + Lay::scr_off(cps));
+    u64 *scr = reinterpret_cast<u64 *>(smem + Lay::scr_off(cps));
+    float *scrf = reinterpret_cast<float *>(scr + 32);               // [8] warp maxima
     float *wev = reinterpret_cast<float *>(smem + Lay::ev_off(cps)) + warp * kP2Batch * 32;
-    float *wb = reinterpret_cast<float *>(smem + Lay::wb_off(cps)) + warp * 32;
+    int *wcum = reinterpret_cast<int *>(smem + Lay::cum_off(cps)) + warp * kP2Batch;
+    int *wlast = reinterpret_cast<int *>(smem + Lay::last_off(cps)) + warp * kP2Batch;
     int *wl = reinterpret_cast<int *>(smem + Lay::wl_off(cps)) + warp * 32;
     float *red = reinterpret_cast<float *>(smem + Lay::red_off(cps));
     float *part = reinterpret_cast<float *>(smem + Lay::part_off(cps));
 
-    cluster_arrive();  // first half of the barrier that makes every CTA's shared memory addressable
+    pdl_launch_dependents();  // the next call's pass 1 may start its prologue on free SMs
+    cluster_arrive();         // first half of the barrier that makes every CTA's shared memory addressable
 
     // Inputs the previous kernel does not write may be read before the dependency wait.
     long long start;
@@ -161,7 +174,6 @@ __global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Para
     const int cw0 = c_lo + warp * kper, cw1 = min(c_hi, cw0 + kper);  // this warp's chunks
     const size_t rec0 = (size_t(b) * p.Hq + hq) * p.nch;
     const float *sseq = p.stash + size_t(hq) * p.total_tokens + start;
-    const float Sf = float(p.S);
 
     float acc[kE];
 #pragma unroll
@@ -192,60 +204,59 @@ __global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Para
             for (int k = 0; k < kP2Batch; ++k) wev[k * 32 + lane] = ev[k];
         }
 
-        // ---- reducer: M, then the scan (as a running maximum) and the threshold counts
+        // ---- reducer: M; then C (fixed point, exact sums) and Z
         float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
         for (int base = kBlk; base < Nb; base += kBlk)
             for (int k = 0; k < kP2Rec; ++k) {
                 const int c = base + tid * kP2Rec + k;
                 if (c < Nb) mx = fmaxf(mx, __ldcg(p.rec_m + rec0 + c));
             }
-        const float M = block_max<kPass2Warps>(mx, scr);
-        float carry = 0.f, carry_max = 0.f;
-        for (int base = 0; base < Nb; base += kBlk) {
+        mx = warp_max(mx);
+        if (lane == 0) scrf[warp] = mx;
+        __syncthreads();
+        float M = scrf[0];
+#pragma unroll
+        for (int w = 1; w < kPass2Warps; ++w) M = fmaxf(M, scrf[w]);
+
+        u64 carry = 0;
+        for (int base = 0, it = 0; base < Nb; base += kBlk, ++it) {
             if (base > 0) load_block(base);
-            float cl[kP2Rec];  // this thread's chunks: local inclusive prefix
-            float run = 0.f;
+            u64 pl[kP2Rec];  // this thread's chunks: local inclusive prefix
+            u64 run = 0;
 #pragma unroll
             for (int k = 0; k < kP2Rec; ++k) {
+                const int c = base + tid * kP2Rec + k;
                 const float st = expf(mr[k] - M);
-                const int c = base + tid * kP2Rec + k;
                 if (c >= c_lo && c < c_hi) s_st[c - c_lo] = st;
-                run += base + tid * kP2Rec + k < Nb ? zr[k] * st : 0.f;
-                cl[k] = run;
+                run += c < Nb ? (u64)__float2ll_rn(zr[k] * st * kMassScale) : 0ull;
+                pl[k] = run;
             }
-            float total;
-            const float incl = block_inclusive_scan<kPass2Warps>(run, scr + 8, &total);
-            const float excl = carry + (incl - run);  // start of this thread's chunks (rounded)
-            float hi = carry_max;
-#pragma unroll
-            for (int k = 0; k < kP2Rec; ++k) hi = fmaxf(hi, excl + cl[k]);
-            const float pre = block_inclusive_max<kPass2Warps>(hi, scr + 16);  // running max up to this thread
+            const u64 incl = warp_inclusive_scan_u64(run, lane);
+            u64 *wsum = scr + (it & 1) * 8;  // alternate slots: no barrier needed before reuse
+            if (lane == 31) wsum[warp] = incl;
             __syncthreads();
-            if (tid == kThreads - 1) scr[32] = pre;
-            // the running max entering this thread: the previous thread's (for lane 0,
-            // the earlier warps' maxima), and the carry from the earlier blocks
-            float before = __shfl_up_sync(kFull, pre, 1);
-            if (lane == 0) {
-                before = carry_max;
-                for (int w = 0; w < warp; ++w) before = fmaxf(before, scr[16 + w]);
+            u64 woff = 0, btot = 0;
+#pragma unroll
+            for (int w = 0; w < kPass2Warps; ++w) {
+                const u64 t = wsum[w];
+                if (w < warp) woff += t;
+                btot += t;
             }
-            before = fmaxf(before, carry_max);
+            const u64 excl = carry + woff + (incl - run);
 #pragma unroll
             for (int k = 0; k < kP2Rec; ++k) {
-                before = fmaxf(before, excl + cl[k]);
                 const int c = base + tid * kP2Rec + k;
-                if (c >= c_lo - 1 && c < c_hi) sC[c - c_lo + 1] = before;
+                if (c >= c_lo - 1 && c < c_hi) sC[c - c_lo + 1] = excl + pl[k];
             }
-            __syncthreads();
-            carry = carry + total;
-            carry_max = scr[32];
+            carry += btot;
         }
-        const float Z = carry_max;  // = C_{N_b - 1}
-        if (c_lo == 0 && tid == 0) sC[0] = 0.f;
+        const u64 Z = carry;  // = C_{N_b - 1}
+        if (c_lo == 0 && tid == 0) sC[0] = 0ull;
         __syncthreads();
 
-        const float SU = Sf * u;
-        for (int i = tid; i <= c_hi - c_lo; i += kThreads) {  // N(C_{c-1}) for c = c_lo .. c_hi
+        // threshold counts: N(C_{c-1}) for c = c_lo .. c_hi (monotone in C)
+        const float Sf = float(p.S), SU = Sf * u, fZ = __ull2float_rn(Z);
+        for (int i = tid; i <= c_hi - c_lo; i += kThreads) {
             const int c = c_lo + i - 1;
             int n;
             if (c < 0)
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Para
             else if (c == Nb - 1)
                 n = p.S;
             else
-                n = int(fminf(fmaxf(ceilf(fmaf(Sf, sC[i] / Z, -SU)), 0.f), Sf));
+                n = int(fminf(fmaxf(ceilf(fmaf(Sf, __ull2float_rn(sC[i]) / fZ, -SU)), 0.f), Sf));
             sN[i] = n;
         }
         __syncthreads();
@@ -273,10 +284,12 @@ __global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Para
             }
         }
 
-        // ---- this warp's chunks with thresholds: in-chunk prefix, systematic search, queued V gather
+        // ---- this warp's chunks, 16 at a time: in-chunk prefixes, the batch's
+        // thresholds one per lane (systematic search), queued V gathers
         const int kvh = hq / p.G;
         const size_t vstride = size_t(p.Hkv) * D;
         const T *vseq = static_cast<const T *>(p.v) + size_t(start) * vstride + size_t(kvh) * D;
+        const double Zd = double(Z), invS = 1.0 / double(p.S);
         int nq = 0;  // keys queued in wl
         auto flush = [&]() {
             __syncwarp();
@@ -286,43 +299,53 @@ __global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Para
             __syncwarp();
         };
         for (int c0 = cw0; c0 < cw1; c0 += kP2Batch) {
-            if (c0 > cw0) {  // later batches: only the chunks that hold a threshold
+            const int kend = min(kP2Batch, cw1 - c0);
+            // samples of the batch's chunks: lane k < kend holds chunk k's count
+            const int my_cnt = lane < kend ? sN[c0 - c_lo + lane + 1] - sN[c0 - c_lo + lane] : 0;
+            if (c0 > cw0) {  // later batches: read only the chunks that hold a threshold
 #pragma unroll
                 for (int k = 0; k < kP2Batch; ++k) {
                     const int c = c0 + k;
                     const int key = c * kChunkRows + lane;
-                    const bool need = c < cw1 && sN[c - c_lo + 1] > sN[c - c_lo];
+                    const bool need = __shfl_sync(kFull, my_cnt, k) > 0;
                     wev[k * 32 + lane] = (need && key < L) ? __ldcg(sseq + key) : 0.f;
                 }
             }
-            __syncwarp();
-            const int kend = min(kP2Batch, cw1 - c0);
-            for (int k = 0; k < kend; ++k) {
-                const int c = c0 + k, i = c - c_lo;
-                const int first = sN[i], cnt = sN[i + 1] - first;
-                if (cnt <= 0) continue;
+            const int cum = warp_inclusive_scan_int(my_cnt, lane);
+            const int total = __shfl_sync(kFull, cum, 31);
+            if (total == 0) continue;
+            if (lane < kP2Batch) wcum[lane] = cum;
+            // in-chunk prefixes of all chunks of the batch (independent scans), in place
+#pragma unroll
+            for (int k = 0; k < kP2Batch; ++k) {
                 const float e = wev[k * 32 + lane];
-                wb[lane] = warp_inclusive_scan(e, lane);
+                const float P = warp_inclusive_scan(e, lane);
                 const unsigned pos = __ballot_sync(kFull, e > 0.f);
-                const int last_pos = pos ? 31 - __clz(pos) : -1;
-                const int len = min(kChunkRows, L - c * kChunkRows);
-                const float Cprev = sC[i], st = s_st[i];
-                __syncwarp();
-                for (int g0 = 0; g0 < cnt; g0 += 32) {
-                    const int nn = min(32, cnt - g0);
-                    if (nq + nn > 32) flush();
-                    if (lane < nn) {
-                        const int m = first + g0 + lane;
-                        const float thr = u + float(m) / Sf;
-                        const float r = (thr * Z - Cprev) / st;
-                        const int j = c * kChunkRows + cdf_search(wb, len, r, last_pos);
-                        wl[nq + lane] = j;
-                        if (p.dbg_idx) p.dbg_idx[(size_t(b) * p.Hq + hq) * p.S + m] = j;
-                    }
-                    nq += nn;
-                }
-                __syncwarp();
+                wev[k * 32 + lane] = P;
+                if (lane == k) wlast[k] = pos ? 31 - __clz(pos) : -1;
             }
+            __syncwarp();
+            for (int g0 = 0; g0 < total; g0 += 32) {
+                const int nn = min(32, total - g0);
+                if (nq + nn > 32) flush();
+                const int g = g0 + lane;
+                if (g < total) {
+                    int k = 0;  // chunk of the batch that holds sample g: first k with cum[k] > g
+#pragma unroll
+                    for (int s = kP2Batch / 2; s > 0; s >>= 1)
+                        if (wcum[k + s - 1] <= g) k += s;
+                    const int c = c0 + k, i = c - c_lo;
+                    const int m = sN[i] + g - (k > 0 ? wcum[k - 1] : 0);
+                    const double t = (double(u) + double(m) * invS) * Zd - double(sC[i]);
+                    const float r = float(t / double(kMassScale)) / s_st[i];
+                    const int len = min(kChunkRows, L - c * kChunkRows);
+                    const int j = c * kChunkRows + cdf_search(wev + k * 32, len, r, wlast[k]);
+                    wl[nq + lane] = j;
+                    if (p.dbg_idx) p.dbg_idx[(size_t(b) * p.Hq + hq) * p.S + m] = j;
+                }
+                nq += nn;
+            }
+            __syncwarp();
         }
         if (nq > 0) flush();
     }
@@ -343,7 +366,7 @@ __global__ void __launch_bounds__(kPass2Warps * 32) prop_pass2_kernel(const Para
     if (split == 0 && tid < D) {
         float s = 0.f;
         for (int k = 0; k < int(gridDim.x); ++k) s += part[k * D + tid];
-        p.out[(size_t(b) * p.Hq + hq) * D + tid] = L > 0 ? s / Sf : 0.f;
+        p.out[(size_t(b) * p.Hq + hq) * D + tid] = L > 0 ? s / float(p.S) : 0.f;
     }
 }
 

@@ -63,7 +63,7 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
         long long grid = sms >= p.Hkv ? (long long)(sms / p.Hkv) * p.Hkv : sms;
         if (grid > chunks) grid = chunks;
         if (tm.begin) cudaEventRecord(tm.begin, stream);
-        e = launch_kernel(k1, dim3(unsigned(grid)), dim3(kChunkWarps * 32), s1, stream, false, 0, kmap32, p, nbuf);
+        e = launch_kernel(k1, dim3(unsigned(grid)), dim3(kChunkWarps * 32), s1, stream, true, 0, kmap32, p, nbuf);
         if (e != cudaSuccess) return e;
         if (tm.end) cudaEventRecord(tm.end, stream);
         return launch_kernel(k2, dim3(p.nsplit, p.Hq, p.B), dim3(kPass2Warps * 32), s2, stream, true, p.nsplit, p);

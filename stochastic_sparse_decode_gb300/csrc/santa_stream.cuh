@@ -30,6 +30,8 @@
 // G * D / 8 > 64 (G = 8 at d = 128) the q slice does not fit in registers and
 // the heads are taken GH at a time, re-reading the buffer.
 //
+// Launched with programmatic dependent launch: a CTA sets up its barriers while
+// the previous kernel drains and waits for it before touching global memory.
 // Every wait is bounded; a timed-out wait raises SANTA_ERR_TIMEOUT (location
 // code 2 in bits 8..11), stops the warp, and lets its copies in flight land.
 #pragma once
@@ -98,23 +100,58 @@ __device__ __forceinline__ float head_sum(float v) {
     return v;
 }
 
-// Where a warp's n-th chunk lies: KV head, chunk of its sequence, and the
-// sequence's (b, start, length), cached from the previous lookup.
+// A warp's walk over its chunks x = W, W + P, W + 2P, ... (x = (b * nch + ch) * Hkv
+// + kvh): KV head, chunk of the sequence and the sequence's (start, length),
+// advanced incrementally -- one 64-bit division when the walk starts, then
+// 32-bit steps -- and the sequence bounds reloaded only when b changes.
 struct ChunkCursor {
-    int b = -1, L = 0;
+    int kvh, ch, b, dk, dr;
+    int L = 0, lb = -1;  // length of sequence lb
     long long start = 0;
-    __device__ __forceinline__ int locate(const Params &p, long long x, int *ch, int *kvh) {
-        *kvh = int(x % p.Hkv);
-        const long long r = x / p.Hkv;
-        *ch = int(r % p.nch);
-        const int bb = int(r / p.nch);
-        if (bb != b) {
-            L = seq_bounds(p, bb, &start);
-            b = bb;
+    __device__ __forceinline__ void init(const Params &p, long long W, long long P) {
+        kvh = int(W % p.Hkv);
+        const long long r = W / p.Hkv;
+        ch = int(r % p.nch);
+        b = int(r / p.nch);
+        dk = int(P % p.Hkv);
+        dr = int(P / p.Hkv);
+    }
+    __device__ __forceinline__ void advance(const Params &p) {
+        kvh += dk;
+        int step = dr;
+        if (kvh >= p.Hkv) {
+            kvh -= p.Hkv;
+            ++step;
         }
-        return min(kChunkRows, L - *ch * kChunkRows);  // keys of the chunk (<= 0: none)
+        const int t = ch + step;  // < nch + P / Hkv + 1, far below 2^31
+        b += t / p.nch;
+        ch = t % p.nch;
+    }
+    // keys of the current chunk (<= 0: none); loads the sequence bounds if b is new
+    __device__ __forceinline__ int len(const Params &p) {
+        if (b >= p.B) return 0;
+        if (b != lb) {
+            L = seq_bounds(p, b, &start);
+            lb = b;
+        }
+        return min(kChunkRows, L - ch * kChunkRows);
     }
 };
+
+// This lane's slice of q for heads h0 .. h0 + GH - 1 of KV head kvh of sequence b:
+// 16-byte column vectors l8, l8 + 8, ... of each head, as float pairs.
+template <typename T, int D, int GH, int VPL, int PAIRS>
+__device__ __forceinline__ void load_q_slice(const Params &p, int b, int hq0, int l8, float2 (&qreg)[GH][VPL * PAIRS]) {
+    using Geo = TileGeom<T, D>;
+    const T *qh = static_cast<const T *>(p.q) + (size_t(b) * p.Hq + hq0) * D;
+#pragma unroll
+    for (int h = 0; h < GH; ++h)
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qh + h * D + (l8 + 8 * i) * Geo::kEV));
+            Vec16<T>::unpack(raw, &qreg[h][i * PAIRS]);
+        }
+}
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kChunkWarps * 32, 1)
@@ -122,6 +159,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     using Geo = TileGeom<T, D>;
     using CG = ChunkGeom<T, D, G>;
     constexpr int kGH = CG::kGH, kVPL = CG::kVPL, kKB = CG::kKB, kPairs = Geo::kPairs;
+    constexpr int kBG = kGH >= 2 ? 2 : 1;  // batches whose partial sums are reduced together
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g8 = lane >> 3, l8 = lane & 7;
     const long long X = (long long)p.B * p.nch * p.Hkv;  // chunks of the batch (with empty ones)
     const long long W = (long long)warp * gridDim.x + blockIdx.x;
@@ -139,37 +177,47 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     if (lane == 0) prefetch_tensormap(&kmap);
     fence_barrier_init();
     __syncwarp();
+    ChunkCursor cur, icur;  // the compute walk and lane 0's issue walk (nbuf chunks ahead)
+    cur.init(p, W, P);
+    icur = cur;
+    // Everything above touches no global memory; the previous kernel in the stream
+    // (which may produce q, K or read this call's workspace) must be complete below.
+    pdl_wait();
 
-    // lane 0: start the copy of this warp's n-th chunk into buffer n % nbuf; a
-    // chunk without keys completes the buffer's phase with a plain arrive.
-    ChunkCursor icur;  // the issuing lane's cursor (it runs nbuf chunks ahead)
+    // lane 0: start the copy of the issue walk's chunk into buffer n % nbuf and step
+    // the walk; a chunk without keys completes the buffer's phase with a plain arrive.
     auto issue = [&](int n) {
-        int ch, kvh;
-        const int len = icur.locate(p, W + n * P, &ch, &kvh);
+        const int len = icur.len(p);
         uint64_t *bar = &bars[n % nbuf];
         if (len > 0) {
             unsigned char *dst = wbuf + size_t(n % nbuf) * CG::kBytes;
             mbar_arrive_expect_tx(bar, CG::kBytes);
 #pragma unroll
             for (int bx = 0; bx < Geo::kBoxes; ++bx)
-                tma_load_3d(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, kvh,
-                            int(icur.start) + ch * kChunkRows);
+                tma_load_3d(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, icur.kvh,
+                            int(icur.start) + icur.ch * kChunkRows);
         } else {
             mbar_arrive(bar);
         }
+        icur.advance(p);
     };
     if (lane == 0)
         for (int n = 0; n < nbuf && n < n_mine; ++n) issue(n);
 
-    ChunkCursor cur;
-    int qb = -1, qkvh = -1;  // whose q the registers hold (one pass only)
+    // q of the first chunk is loaded while its keys are in flight
     float2 qreg[kGH][kVPL * kPairs];
+    int qb = -1, qkvh = -1;  // whose q the registers hold (one pass only)
+    if (CG::kPasses == 1 && n_mine > 0 && cur.b < p.B) {
+        load_q_slice<T, D, kGH, kVPL, kPairs>(p, cur.b, cur.kvh * G, l8, qreg);
+        qb = cur.b;
+        qkvh = cur.kvh;
+    }
+
     int n = 0;
     bool failed = false;
-    for (; n < n_mine; ++n) {
-        int ch, kvh;
-        const int len = cur.locate(p, W + n * P, &ch, &kvh);
-        const int b = cur.b;
+    for (; n < n_mine; ++n, cur.advance(p)) {
+        const int len = cur.len(p);
+        const int b = cur.b, kvh = cur.kvh, ch = cur.ch;
         if (!mbar_wait(&bars[n % nbuf], (n / nbuf) & 1)) {
             failed = true;
             break;
@@ -183,49 +231,50 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
 #pragma unroll
         for (int hp = 0; hp < CG::kPasses; ++hp) {
             if (CG::kPasses > 1 || b != qb || kvh != qkvh) {
-                const T *qh = static_cast<const T *>(p.q) + (size_t(b) * p.Hq + size_t(kvh) * G + hp * kGH) * D;
-#pragma unroll
-                for (int h = 0; h < kGH; ++h)
-#pragma unroll
-                    for (int i = 0; i < kVPL; ++i) {
-                        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qh + h * D + (l8 + 8 * i) * Geo::kEV));
-                        Vec16<T>::unpack(raw, &qreg[h][i * kPairs]);
-                    }
+                load_q_slice<T, D, kGH, kVPL, kPairs>(p, b, kvh * G + hp * kGH, l8, qreg);
                 qb = b;
                 qkvh = kvh;
             }
             float x[kGH];  // logit of this lane's key of batch bt, head l8 % GH of the pass
 #pragma unroll
-            for (int bt = 0; bt < kGH; ++bt) {  // batches of kKB keys per lane group
-                float v[8];
+            for (int bg = 0; bg < kGH; bg += kBG) {  // kBG batches of kKB keys per lane group
+                float v[kBG][8];
 #pragma unroll
-                for (int kk = 0; kk < kKB; ++kk) {
-                    const int r = bt * 4 * kKB + g8 * kKB + kk;  // row of the chunk
-                    float2 acc[kGH];
+                for (int bb = 0; bb < kBG; ++bb)
 #pragma unroll
-                    for (int h = 0; h < kGH; ++h) acc[h] = make_float2(0.f, 0.f);
+                    for (int kk = 0; kk < kKB; ++kk) {
+                        const int r = (bg + bb) * 4 * kKB + g8 * kKB + kk;  // row of the chunk
+                        float2 acc[kGH];
 #pragma unroll
-                    for (int i = 0; i < kVPL; ++i) {
-                        // 16-byte vector l8 + 8i of row r: box i, swizzled position l8 ^ (r mod 8)
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(base + i * kChunkBoxBytes + r * 128 +
-                                                                           ((l8 ^ (r & 7)) << 4));
-                        float2 kv[kPairs];
-                        Vec16<T>::unpack(raw, kv);
+                        for (int h = 0; h < kGH; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int h = 0; h < kGH; ++h)
+                        for (int i = 0; i < kVPL; ++i) {
+                            // 16-byte vector l8 + 8i of row r: box i, swizzled position l8 ^ (r mod 8)
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(base + i * kChunkBoxBytes + r * 128 +
+                                                                               ((l8 ^ (r & 7)) << 4));
+                            float2 kv[kPairs];
+                            Vec16<T>::unpack(raw, kv);
 #pragma unroll
-                            for (int pp = 0; pp < kPairs; ++pp)
-                                acc[h] = __ffma2_rn(qreg[h][i * kPairs + pp], kv[pp], acc[h]);
+                            for (int h = 0; h < kGH; ++h)
+#pragma unroll
+                                for (int pp = 0; pp < kPairs; ++pp)
+                                    acc[h] = __ffma2_rn(qreg[h][i * kPairs + pp], kv[pp], acc[h]);
+                        }
+#pragma unroll
+                        for (int h = 0; h < kGH; ++h) v[bb][kk * kGH + h] = acc[h].x + acc[h].y;
                     }
+                // lane l8 of the group ends with value l8 of each batch: key l8 / GH, head l8 % GH
 #pragma unroll
-                    for (int h = 0; h < kGH; ++h) v[kk * kGH + h] = acc[h].x + acc[h].y;
+                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<4>(v[bb], l8);
+#pragma unroll
+                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<2>(v[bb], l8);
+#pragma unroll
+                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<1>(v[bb], l8);
+#pragma unroll
+                for (int bb = 0; bb < kBG; ++bb) {
+                    const int key = (bg + bb) * 4 * kKB + g8 * kKB + l8 / kGH;
+                    x[bg + bb] = key < len ? v[bb][0] * p.scale : -INFINITY;
                 }
-                // lane l8 of the group ends with value l8: key l8 / GH of the batch, head l8 % GH
-                reduce_scatter_stage<4>(v, l8);
-                reduce_scatter_stage<2>(v, l8);
-                reduce_scatter_stage<1>(v, l8);
-                const int key = bt * 4 * kKB + g8 * kKB + l8 / kGH;
-                x[bt] = key < len ? v[0] * p.scale : -INFINITY;
             }
             if (hp == CG::kPasses - 1) {
                 // Every lane is done with the buffer: refill it with chunk n + nbuf.
