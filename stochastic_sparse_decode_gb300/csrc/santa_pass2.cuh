@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
         const int kvh = hq / p.G;
         const size_t vstride = size_t(p.Hkv) * D;
         const T *vseq = static_cast<const T *>(p.v) + size_t(start) * vstride + size_t(kvh) * D;
-        const double Zd = double(Z), invS = 1.0 / double(p.S);
+        const float Zf = fZ / kMassScale, invS = 1.0f / Sf;  // Z on the mass scale
         int nq = 0;  // keys queued in wl
         auto flush = [&]() {
             __syncwarp();
@@ -315,15 +315,27 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
             const int total = __shfl_sync(kFull, cum, 31);
             if (total == 0) continue;
             if (lane < kP2Batch) wcum[lane] = cum;
-            // in-chunk prefixes of all chunks of the batch (independent scans), in place
+            // in-chunk prefixes of all chunks of the batch: 16 independent scans,
+            // all loads first so that their latencies overlap, written back in place
+            float ev[kP2Batch];
+#pragma unroll
+            for (int k = 0; k < kP2Batch; ++k) ev[k] = wev[k * 32 + lane];
+            unsigned last_pos = 0;  // lane k: last positive key of chunk k
 #pragma unroll
             for (int k = 0; k < kP2Batch; ++k) {
-                const float e = wev[k * 32 + lane];
-                const float P = warp_inclusive_scan(e, lane);
-                const unsigned pos = __ballot_sync(kFull, e > 0.f);
-                wev[k * 32 + lane] = P;
-                if (lane == k) wlast[k] = pos ? 31 - __clz(pos) : -1;
+                const unsigned pos = __ballot_sync(kFull, ev[k] > 0.f);
+                if (lane == k) last_pos = pos;
             }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+                for (int k = 0; k < kP2Batch; ++k) {
+                    const float t = __shfl_up_sync(kFull, ev[k], o);
+                    if (lane >= o) ev[k] += t;
+                }
+#pragma unroll
+            for (int k = 0; k < kP2Batch; ++k) wev[k * 32 + lane] = ev[k];
+            if (lane < kP2Batch) wlast[lane] = last_pos ? 31 - __clz(last_pos) : -1;
             __syncwarp();
             for (int g0 = 0; g0 < total; g0 += 32) {
                 const int nn = min(32, total - g0);
@@ -336,8 +348,8 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
                         if (wcum[k + s - 1] <= g) k += s;
                     const int c = c0 + k, i = c - c_lo;
                     const int m = sN[i] + g - (k > 0 ? wcum[k - 1] : 0);
-                    const double t = (double(u) + double(m) * invS) * Zd - double(sC[i]);
-                    const float r = float(t / double(kMassScale)) / s_st[i];
+                    const float thr = fmaf(float(m), invS, u);
+                    const float r = fmaf(thr, Zf, -__ull2float_rn(sC[i]) / kMassScale) / s_st[i];
                     const int len = min(kChunkRows, L - c * kChunkRows);
                     const int j = c * kChunkRows + cdf_search(wev + k * 32, len, r, wlast[k]);
                     wl[nq + lane] = j;

@@ -11,21 +11,25 @@
 // on how finely the records cut the keys, and chunk records let every warp
 // finish its keys on its own.
 //
-// Launched as one CTA of kChunkWarps warps per SM.  Chunks are numbered
-// (sequence, chunk, KV head) with the KV head fastest; warp w of CTA c takes
-// chunks W, W + P, W + 2P, ... with W = w C + c and P = C * kChunkWarps (C CTAs,
-// a multiple of Hkv, so a warp keeps one KV head and its q slice stays in
-// registers).  Each warp streams its chunks through `nbuf` shared-memory
-// buffers of its own, filled by 3-D TMA boxes (32 rows x 128 bytes, 128-byte
-// swizzle) that its lane 0 issues, one mbarrier per buffer: no warp ever waits
-// for another.
+// Launched as one CTA of kChunkWarps warps per SM (C CTAs, a multiple of Hkv).
+// Chunks are numbered (sequence, chunk, KV head) with the KV head fastest; CTA
+// c owns chunks c, c + C, c + 2C, ... (so all of them have one KV head and the
+// CTAs move along the token rows together), and its warps claim them one at a
+// time from a shared-memory counter, so the CTA's chunks, not a fixed share per
+// warp, balance the work.  Each warp streams its claims through `nbuf`
+// shared-memory buffers of its own, filled by 3-D TMA boxes (32 rows x 128
+// bytes, 128-byte swizzle) that its lane 0 issues, one mbarrier per buffer: no
+// warp ever waits for another.  A warp starts with one copy in flight and fills
+// its other buffers when that copy lands, so every warp's first chunk is among
+// the first bytes the memory system returns.
 //
 // Eight lanes share a key: lane l of a lane group holds q's slice of 16-byte
 // column vectors l, l + 8, ... (the swizzle makes the eight reads of one row
 // conflict-free), widens bf16 to fp32 and accumulates with packed fp32 FMA.
 // A batch of 8/GH keys x GH heads gives 8 partial sums per lane, which three
-// shuffle stages reduce-scatter over the lane group, so each lane ends with
-// one full logit.  The chunk's statistics are then warp shuffles over the
+// shuffle-and-add stages reduce-scatter over the lane group, so each lane ends
+// with one full logit (each lane orders its heads and keys by its own index,
+// so no stage needs a select).  The chunk's statistics are then warp shuffles over the
 // lanes that hold the same head; e is stored straight to the stash.  With
 // G * D / 8 > 64 (G = 8 at d = 128) the q slice does not fit in registers and
 // the heads are taken GH at a time, re-reading the buffer.
@@ -46,6 +50,12 @@ constexpr int kChunkWarps = 12;                     // warps of a pass-1 CTA
 constexpr int kChunkMaxBuf = 4;                     // buffers per warp, at most
 constexpr int kChunkBoxBytes = kChunkRows * 128;    // one TMA box: 32 rows x 128 bytes
 
+// What a buffer holds: chunk ch of sequence b (rows start + 32 ch ..), KV head, keys.
+struct ChunkSlot {
+    long long start;
+    int b, ch, kvh, len;
+};
+
 template <typename T, int D, int G>
 struct ChunkGeom {
     using Geo = TileGeom<T, D>;
@@ -54,11 +64,14 @@ struct ChunkGeom {
     static constexpr int kBytes = Geo::kBoxes * kChunkBoxBytes;       // one chunk of K rows
     static constexpr int kVPL = Geo::kNJ / 8;  // 16-byte vectors of a row per lane (8 lanes per key)
     static constexpr int kKB = 8 / kGH;        // keys per lane group in one reduction batch
-    // shared memory: [kChunkWarps][nbuf] chunk buffers, then the buffers' mbarriers
+    // shared memory: [kChunkWarps][nbuf] chunk buffers, [kChunkWarps][kChunkMaxBuf]
+    // mbarriers, [kChunkWarps][kChunkMaxBuf] slot descriptors, the claim counter
     static __host__ __device__ size_t bars_off(int nbuf) { return size_t(kChunkWarps) * nbuf * kBytes; }
-    static __host__ __device__ size_t bytes(int nbuf) {
-        return 1024 + bars_off(nbuf) + size_t(kChunkWarps) * kChunkMaxBuf * 8;
+    static __host__ __device__ size_t slots_off(int nbuf) { return bars_off(nbuf) + size_t(kChunkWarps) * kChunkMaxBuf * 8; }
+    static __host__ __device__ size_t next_off(int nbuf) {
+        return slots_off(nbuf) + size_t(kChunkWarps) * kChunkMaxBuf * sizeof(ChunkSlot);
     }
+    static __host__ __device__ size_t bytes(int nbuf) { return 1024 + next_off(nbuf) + 16; }
     // buffers per warp that fit in `optin` bytes of shared memory (0: none)
     static __host__ int nbuf_for(size_t optin) {
         for (int n = kChunkMaxBuf; n >= 1; --n)
@@ -71,18 +84,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// One stage of a reduce-scatter over the 8 lanes of a lane group: the lanes
-// with bit M set keep values [M, 2M) of v and hand [0, M) to their partner
-// (lane ^ M), the others the reverse; afterwards v[0, M) holds the partner sums.
+// One stage of a reduce-scatter over the 8 lanes of a lane group.  Slot s of
+// lane l holds the partial sum of value s ^ l (each lane keeps its values in an
+// order permuted by its own index), so for every stage the lane keeps slots
+// [0, M) and hands slots [M, 2M) to its partner l ^ M, whose slot j + M holds
+// the same value as this lane's slot j.  After the stages 4, 2, 1 slot 0 of
+// lane l holds the full sum of value l.
 template <int M>
-__device__ __forceinline__ void reduce_scatter_stage(float (&v)[8], int l8) {
-    const bool upper = (l8 & M) != 0;
+__device__ __forceinline__ void reduce_scatter_stage(float (&v)[8]) {
 #pragma unroll
-    for (int j = 0; j < M; ++j) {
-        const float lo = v[j], hi = v[j + M];
-        const float recv = __shfl_xor_sync(kFull, upper ? lo : hi, M);
-        v[j] = (upper ? hi : lo) + recv;
-    }
+    for (int j = 0; j < M; ++j) v[j] += __shfl_xor_sync(kFull, v[j + M], M);
 }
 
 // Max / sum over the lanes that hold the same head: lanes whose indices differ
@@ -100,55 +111,19 @@ __device__ __forceinline__ float head_sum(float v) {
     return v;
 }
 
-// A warp's walk over its chunks x = W, W + P, W + 2P, ... (x = (b * nch + ch) * Hkv
-// + kvh): KV head, chunk of the sequence and the sequence's (start, length),
-// advanced incrementally -- one 64-bit division when the walk starts, then
-// 32-bit steps -- and the sequence bounds reloaded only when b changes.
-struct ChunkCursor {
-    int kvh, ch, b, dk, dr;
-    int L = 0, lb = -1;  // length of sequence lb
-    long long start = 0;
-    __device__ __forceinline__ void init(const Params &p, long long W, long long P) {
-        kvh = int(W % p.Hkv);
-        const long long r = W / p.Hkv;
-        ch = int(r % p.nch);
-        b = int(r / p.nch);
-        dk = int(P % p.Hkv);
-        dr = int(P / p.Hkv);
-    }
-    __device__ __forceinline__ void advance(const Params &p) {
-        kvh += dk;
-        int step = dr;
-        if (kvh >= p.Hkv) {
-            kvh -= p.Hkv;
-            ++step;
-        }
-        const int t = ch + step;  // < nch + P / Hkv + 1, far below 2^31
-        b += t / p.nch;
-        ch = t % p.nch;
-    }
-    // keys of the current chunk (<= 0: none); loads the sequence bounds if b is new
-    __device__ __forceinline__ int len(const Params &p) {
-        if (b >= p.B) return 0;
-        if (b != lb) {
-            L = seq_bounds(p, b, &start);
-            lb = b;
-        }
-        return min(kChunkRows, L - ch * kChunkRows);
-    }
-};
-
-// This lane's slice of q for heads h0 .. h0 + GH - 1 of KV head kvh of sequence b:
-// 16-byte column vectors l8, l8 + 8, ... of each head, as float pairs.
+// This lane's slice of q for heads h0 .. h0 + GH - 1 of sequence b: 16-byte
+// column vectors l8, l8 + 8, ... of each head, as float pairs; slot h holds
+// head h0 + (h ^ hx) (the lane's head permutation of the reduce-scatter).
 template <typename T, int D, int GH, int VPL, int PAIRS>
-__device__ __forceinline__ void load_q_slice(const Params &p, int b, int hq0, int l8, float2 (&qreg)[GH][VPL * PAIRS]) {
+__device__ __forceinline__ void load_q_slice(const Params &p, int b, int hq0, int l8, int hx,
+                                             float2 (&qreg)[GH][VPL * PAIRS]) {
     using Geo = TileGeom<T, D>;
     const T *qh = static_cast<const T *>(p.q) + (size_t(b) * p.Hq + hq0) * D;
 #pragma unroll
     for (int h = 0; h < GH; ++h)
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qh + h * D + (l8 + 8 * i) * Geo::kEV));
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qh + (h ^ hx) * D + (l8 + 8 * i) * Geo::kEV));
             Vec16<T>::unpack(raw, &qreg[h][i * PAIRS]);
         }
 }
@@ -161,77 +136,124 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     constexpr int kGH = CG::kGH, kVPL = CG::kVPL, kKB = CG::kKB, kPairs = Geo::kPairs;
     constexpr int kBG = kGH >= 2 ? 2 : 1;  // batches whose partial sums are reduced together
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g8 = lane >> 3, l8 = lane & 7;
+    // the lane's permutation of its reduce-scatter slots (kk, h) -> (kk ^ kx, h ^ hx)
+    const int hx = l8 & (kGH - 1), kx = l8 / kGH;
+    const int C = gridDim.x, c = blockIdx.x;
     const long long X = (long long)p.B * p.nch * p.Hkv;  // chunks of the batch (with empty ones)
-    const long long W = (long long)warp * gridDim.x + blockIdx.x;
-    const long long P = (long long)gridDim.x * kChunkWarps;
-    const int n_mine = W < X ? int((X - W + P - 1) / P) : 0;
+    const long long K_cta = X > c ? (X - c + C - 1) / C : 0;  // chunks c, c + C, ... of this CTA
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~uintptr_t(1023));
     unsigned char *wbuf = smem + size_t(warp) * nbuf * CG::kBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CG::bars_off(nbuf)) + warp * kChunkMaxBuf;
+    ChunkSlot *slots = reinterpret_cast<ChunkSlot *>(smem + CG::slots_off(nbuf)) + warp * kChunkMaxBuf;
+    int *s_next = reinterpret_cast<int *>(smem + CG::next_off(nbuf));
 
     pdl_launch_dependents();
     if (lane < nbuf) mbar_init(&bars[lane], 1);
-    if (lane == 0) prefetch_tensormap(&kmap);
+    if (threadIdx.x == 0) {
+        *s_next = 0;
+        prefetch_tensormap(&kmap);
+    }
     fence_barrier_init();
-    __syncwarp();
-    ChunkCursor cur, icur;  // the compute walk and lane 0's issue walk (nbuf chunks ahead)
-    cur.init(p, W, P);
-    icur = cur;
-    // Everything above touches no global memory; the previous kernel in the stream
-    // (which may produce q, K or read this call's workspace) must be complete below.
+    __syncthreads();
+    // Nothing above touches global memory; the previous kernel in the stream (which
+    // may produce q, K or read this call's workspace) must be complete below.
     pdl_wait();
 
-    // lane 0: start the copy of the issue walk's chunk into buffer n % nbuf and step
-    // the walk; a chunk without keys completes the buffer's phase with a plain arrive.
-    auto issue = [&](int n) {
-        const int len = icur.len(p);
-        uint64_t *bar = &bars[n % nbuf];
-        if (len > 0) {
-            unsigned char *dst = wbuf + size_t(n % nbuf) * CG::kBytes;
-            mbar_arrive_expect_tx(bar, CG::kBytes);
-#pragma unroll
-            for (int bx = 0; bx < Geo::kBoxes; ++bx)
-                tma_load_3d(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, icur.kvh,
-                            int(icur.start) + icur.ch * kChunkRows);
-        } else {
-            mbar_arrive(bar);
+    // lane 0's cache of the last sequence's bounds
+    int lb = -1, lL = 0;
+    long long lstart = 0;
+    const bool one_kvh = C % p.Hkv == 0;  // every chunk of the CTA has KV head c % Hkv
+    int n_issued = 0, n_done = 0;
+    bool more = true;  // warp-uniform: the CTA's walk still has chunks to claim
+    // Claims the next chunk of the CTA's walk and starts its copy into buffer
+    // n_issued % nbuf; a chunk without keys completes the buffer's phase with a
+    // plain arrive.  Warp-uniform.
+    auto claim = [&]() {
+        int i = 0;
+        if (lane == 0) i = atomicAdd(s_next, 1);
+        i = __shfl_sync(kFull, i, 0);
+        if (i >= K_cta) {
+            more = false;
+            return;
         }
-        icur.advance(p);
+        if (lane == 0) {
+            int kvh;
+            long long r;  // b * nch + ch
+            if (one_kvh) {
+                kvh = c % p.Hkv;
+                r = c / p.Hkv + (long long)i * (C / p.Hkv);
+            } else {
+                const long long x = c + (long long)i * C;
+                kvh = int(x % p.Hkv);
+                r = x / p.Hkv;
+            }
+            int b, ch;
+            if (r < 0x7fffffffLL) {
+                b = int(unsigned(r) / unsigned(p.nch));
+                ch = int(r) - b * p.nch;
+            } else {
+                b = int(r / p.nch);
+                ch = int(r - (long long)b * p.nch);
+            }
+            if (b != lb) {
+                lL = seq_bounds(p, b, &lstart);
+                lb = b;
+            }
+            const int len = min(kChunkRows, lL - ch * kChunkRows);
+            const int slot = n_issued % nbuf;
+            slots[slot] = ChunkSlot{lstart, b, ch, kvh, len};
+            uint64_t *bar = &bars[slot];
+            if (len > 0) {
+                unsigned char *dst = wbuf + size_t(slot) * CG::kBytes;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, CG::kBytes);
+#pragma unroll
+                for (int bx = 0; bx < Geo::kBoxes; ++bx)
+                    tma_load_3d(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, kvh,
+                                int(lstart) + ch * kChunkRows);
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+        ++n_issued;
     };
-    if (lane == 0)
-        for (int n = 0; n < nbuf && n < n_mine; ++n) issue(n);
+    claim();  // one copy per warp at first
+    __syncwarp();
 
     // q of the first chunk is loaded while its keys are in flight
     float2 qreg[kGH][kVPL * kPairs];
     int qb = -1, qkvh = -1;  // whose q the registers hold (one pass only)
-    if (CG::kPasses == 1 && n_mine > 0 && cur.b < p.B) {
-        load_q_slice<T, D, kGH, kVPL, kPairs>(p, cur.b, cur.kvh * G, l8, qreg);
-        qb = cur.b;
-        qkvh = cur.kvh;
+    if (CG::kPasses == 1 && n_issued > 0) {
+        qb = slots[0].b;
+        qkvh = slots[0].kvh;
+        load_q_slice<T, D, kGH, kVPL, kPairs>(p, qb, qkvh * G, l8, hx, qreg);
     }
 
-    int n = 0;
     bool failed = false;
-    for (; n < n_mine; ++n, cur.advance(p)) {
-        const int len = cur.len(p);
-        const int b = cur.b, kvh = cur.kvh, ch = cur.ch;
-        if (!mbar_wait(&bars[n % nbuf], (n / nbuf) & 1)) {
+    while (n_done < n_issued) {
+        const int slot = n_done % nbuf;
+        if (!mbar_wait(&bars[slot], (n_done / nbuf) & 1)) {
             failed = true;
             break;
         }
+        if (n_done == 0)  // the first copy has landed: fill the other buffers
+            while (more && n_issued < nbuf) claim();
+        const ChunkSlot cs = slots[slot];
+        const int len = cs.len, b = cs.b, kvh = cs.kvh, ch = cs.ch;
         if (len <= 0) {  // nothing to read: pass the buffer on
-            if (lane == 0 && n + nbuf < n_mine) issue(n + nbuf);
+            ++n_done;
+            if (more) claim();
             continue;
         }
-        const unsigned char *base = wbuf + size_t(n % nbuf) * CG::kBytes;
-        const long long row0 = cur.start + (long long)ch * kChunkRows;
+        const unsigned char *base = wbuf + size_t(slot) * CG::kBytes;
+        const long long row0 = cs.start + (long long)ch * kChunkRows;
 #pragma unroll
         for (int hp = 0; hp < CG::kPasses; ++hp) {
             if (CG::kPasses > 1 || b != qb || kvh != qkvh) {
-                load_q_slice<T, D, kGH, kVPL, kPairs>(p, b, kvh * G + hp * kGH, l8, qreg);
+                load_q_slice<T, D, kGH, kVPL, kPairs>(p, b, kvh * G + hp * kGH, l8, hx, qreg);
                 qb = b;
                 qkvh = kvh;
             }
@@ -243,7 +265,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 for (int bb = 0; bb < kBG; ++bb)
 #pragma unroll
                     for (int kk = 0; kk < kKB; ++kk) {
-                        const int r = (bg + bb) * 4 * kKB + g8 * kKB + kk;  // row of the chunk
+                        const int r = (bg + bb) * 4 * kKB + g8 * kKB + (kk ^ kx);  // row of slot (kk, .)
                         float2 acc[kGH];
 #pragma unroll
                         for (int h = 0; h < kGH; ++h) acc[h] = make_float2(0.f, 0.f);
@@ -265,11 +287,11 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                     }
                 // lane l8 of the group ends with value l8 of each batch: key l8 / GH, head l8 % GH
 #pragma unroll
-                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<4>(v[bb], l8);
+                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<4>(v[bb]);
 #pragma unroll
-                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<2>(v[bb], l8);
+                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<2>(v[bb]);
 #pragma unroll
-                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<1>(v[bb], l8);
+                for (int bb = 0; bb < kBG; ++bb) reduce_scatter_stage<1>(v[bb]);
 #pragma unroll
                 for (int bb = 0; bb < kBG; ++bb) {
                     const int key = (bg + bb) * 4 * kKB + g8 * kKB + l8 / kGH;
@@ -277,12 +299,9 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 }
             }
             if (hp == CG::kPasses - 1) {
-                // Every lane is done with the buffer: refill it with chunk n + nbuf.
+                // Every lane is done with the buffer: refill it with the next claim.
                 __syncwarp();
-                if (lane == 0 && n + nbuf < n_mine) {
-                    fence_proxy_async_smem();
-                    issue(n + nbuf);
-                }
+                if (more) claim();
             }
 
             // chunk statistics of the pass's heads; e to the stash, (m_c, z_c) to the records
@@ -309,16 +328,16 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 p.rec_z[rec] = z;
             }
         }
+        ++n_done;
     }
 
     if (failed) {
         // SANTA_ERR_TIMEOUT with location code 2 (a chunk copy never completed);
-        // wait, bounded, for this warp's copies still in flight (chunks n ..
-        // n + nbuf - 1 at most) before exiting.
+        // wait, bounded, for this warp's copies still in flight before exiting.
         if (lane == 0) {
             raise_flag(p, SANTA_ERR_TIMEOUT | (2u << 8));
             const long long t0 = clock64();
-            for (int k = n; k < n_mine && k < n + nbuf; ++k)
+            for (int k = n_done; k < n_issued; ++k)
                 while (!mbar_try_wait(&bars[k % nbuf], (k / nbuf) & 1) && clock64() - t0 < kWaitCycles) {
                 }
         }
