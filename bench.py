@@ -50,7 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=15000)
     ap.add_argument("--warmup", type=int, default=500)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["prop", "flash", "exact"], default="prop")
+    ap.add_argument("--mode", choices=["prop", "strat", "iid", "flash", "exact"], default="prop")
     ap.add_argument("--workload", default="llama8b_32k_b1")
     ap.add_argument("--S", type=int, default=0, help="override the workload's sample count")
     ap.add_argument("--graph-steps", type=int, default=100)
@@ -276,6 +276,10 @@ def run_ours(args, dist: Dist):
         w = w.with_(S=2048)  # the flash mode's configuration (6.25% of n_k)
     inp = generate(w)
     q, k, v, indptr, U = to_torch(inp, dev)
+    if args.mode in ("strat", "iid"):  # the samplers' uniforms [B][Hq][S]
+        from synthetic.workloads import draw_uniforms
+
+        U = torch.from_numpy(draw_uniforms((w.batch, w.num_q_heads, w.S), np.random.default_rng(11))).to(dev)
     dec = Decoder(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, inp.total_tokens, max_length(w), w.tile,
                   w.S, w.dtype, device=dev)
     out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
@@ -286,7 +290,7 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
     sidx = bufs.get("sample_idx")
     sidx = sidx.cpu().numpy().reshape(w.batch, w.num_q_heads, -1) if sidx is not None else None
-    bm = byte_model(inp, args.mode, w.S, sidx)
+    bm = byte_model(inp, "prop" if args.mode in ("strat", "iid") else args.mode, w.S, sidx)
 
     # L2-safe rotation of the K/V cache
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -366,7 +370,8 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
     main_us = statistics.mean(a_.elapsed_time(b_) * 1000.0 for a_, b_ in evs[10:])
     peak, peak_kind = measured_peaks()
-    kernel_name = {"prop": "prop_pass1", "flash": "flash_tile", "exact": "exact_tile"}[args.mode]
+    kernel_name = {"prop": "prop_pass1", "strat": "prop_pass1", "iid": "prop_pass1", "flash": "flash_tile",
+                   "exact": "exact_tile"}[args.mode]
     achieved = bm["main"] / (main_us * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(kernel_name, w.name),
@@ -421,6 +426,15 @@ def run_ours(args, dist: Dist):
             ms, _ = timed(n_x, min(args.warmup, 200), mode="flash", decoder=decf, Uarg=Uf)
             extras["flash_S2048_us_per_layer_step"] = round(ms * 1000.0 / n_x, 3)
             del wf
+        # the prop pipeline with the stratified and i.i.d. samplers, same S
+        from synthetic.workloads import draw_uniforms
+
+        Uu = torch.from_numpy(draw_uniforms((w.batch, w.num_q_heads, w.S), np.random.default_rng(11))).to(dev)
+        for smode in ("strat", "iid"):
+            for i in range(nrot):
+                dec(smode, q, ks[i], vs[i], indptr, Uu, out=out)
+            ms, _ = timed(n_x, min(args.warmup, 200), mode=smode, Uarg=Uu)
+            extras[f"{smode}_us_per_layer_step"] = round(ms * 1000.0 / n_x, 3)
 
     launches_per_step = 2
     res = {
@@ -469,7 +483,11 @@ def _oracle_head(oracle, inp, kv, mode, S, b, h):
     K, V = kv[(b, h // w.group)]
     qh = np.ascontiguousarray(inp.q[b, h], dtype=np.float64)
     U = float(inp.U[0, b, h])
-    if mode == "prop":
+    if mode in ("strat", "iid"):
+        from synthetic.workloads import draw_uniforms
+
+        oracle.sampled_head(mode, qh, K, V, draw_uniforms(S, np.random.default_rng(11 + h)))
+    elif mode == "prop":
         oracle.prop_head(qh, K, V, S, U, w.tile, want_F=False)
     elif mode == "flash":
         oracle.flash_head(qh, K, V, S, U, w.tile)

@@ -151,6 +151,31 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
                       santa_stream_t stream);
 
 /*
+ * The prop pipeline with the two other samplers of the same notes (Key design 1):
+ *
+ *   santa_decode_prop_strat   S2ANTA-strat: threshold m is (m + u_m) / S, one
+ *                             uniform draw inside each stratum [m/S, (m+1)/S);
+ *   santa_decode_prop_iid     SANTA: S independent draws, threshold s is u_s;
+ *                             the samples are taken in increasing order of u.
+ *
+ * u: device [B][Hq][S] float32, each in [0, 1) (a value outside is clamped into
+ * it and raises SANTA_ERR_OFFSET).  out = (1/S) sum V[J], as for prop.  Every
+ * other argument, layout, workspace (santa_workspace_size with SANTA_MODE_PROP),
+ * ownership and error are those of santa_decode_prop; dbg->sample_idx holds, per
+ * (b, h), the key chosen for threshold m (strat) or for the m-th smallest u (iid).
+ * Supported for S <= 16384 (the head's uniforms are kept in shared memory; a
+ * larger S is SANTA_UNSUPPORTED).
+ */
+int santa_decode_prop_strat(const santa_problem *p, const void *q, const void *k, const void *v,
+                            const long long *kv_indptr, const float *u, float *out,
+                            void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                            santa_stream_t stream);
+int santa_decode_prop_iid(const santa_problem *p, const void *q, const void *k, const void *v,
+                          const long long *kv_indptr, const float *u, float *out,
+                          void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                          santa_stream_t stream);
+
+/*
  * S2ANTA-flash decode (paper notes, Key design 3): S_loc = ceil(S / T_b)
  * samples per tile with the shared offset U * S / S_loc, then a merge with
  * weights Z_tile / Z.  Same arguments as santa_decode_prop.

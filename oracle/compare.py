@@ -17,7 +17,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import cdf, exact_head, flash_head, gather_mean, logits, prop_head
+from . import cdf, exact_head, flash_head, gather_mean, logits, prop_head, sampled_head, softmax
 
 IDX_REL = 1e-5
 MASS_REL = 1e-3
@@ -146,6 +146,41 @@ def check_exact_head(q, K, V, gpu_out, what="exact") -> Report:
     rep = Report(heads=1)
     expect = exact_head(q, K, V)
     err = float(np.max(np.abs(np.asarray(gpu_out, dtype=np.float64) - expect)))
+    rep.max_out_err = err
+    assert err <= OUT_ABS, f"{what}: out err {err:.3e}"
+    return rep
+
+
+def check_sampled_head(mode, q, K, V, u, gpu_out, gpu_idx, what=None) -> Report:
+    """One (sequence, query head) of the prop pipeline with the stratified ('strat') or
+    i.i.d. ('iid') sampler and caller uniforms u[S].  strat: gpu_idx[m] is the key of
+    threshold (m + u_m)/S; iid: gpu_idx[m] is the key of the m-th smallest u."""
+    what = what or mode
+    S = int(np.asarray(u).size)
+    rep = Report(heads=1, samples=S)
+    n = K.shape[0]
+    gpu_out = np.asarray(gpu_out, dtype=np.float64)
+    if n == 0:
+        assert np.all(gpu_out == 0.0), f"{what}: empty sequence must give zeros"
+        return rep
+    u = np.asarray(u, dtype=np.float64)
+    ref_out, ref_J = sampled_head(mode, q, K, V, u)
+    if mode == "strat":
+        t = (np.arange(S, dtype=np.float64) + u) / S
+        J = ref_J
+    else:  # threshold order: increasing u (F^-1 is monotone, so J follows)
+        order = np.argsort(u, kind="stable")
+        t, J = u[order], ref_J[order]
+    idx = np.asarray(gpu_idx, dtype=np.int64)
+    assert idx.min() >= 0 and idx.max() < n, f"{what}: index out of range"
+    F = cdf(softmax(logits(q, K)))
+    bad = np.nonzero(idx != J)[0]
+    for m in bad:
+        assert _excused(F, t[m], int(idx[m]), int(J[m])), (
+            f"{what}: sample {m} picked {idx[m]}, oracle {J[m]}, threshold {t[m]!r}")
+    rep.excused += bad.size
+    expect = ref_out if bad.size == 0 else gather_mean(idx, V)
+    err = float(np.max(np.abs(gpu_out - expect)))
     rep.max_out_err = err
     assert err <= OUT_ABS, f"{what}: out err {err:.3e}"
     return rep

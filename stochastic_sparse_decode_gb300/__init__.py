@@ -26,6 +26,8 @@ ERR_INDPTR, ERR_OFFSET, ERR_TIMEOUT = 1, 2, 4
 EXPORTS = (
     "santa_workspace_size",
     "santa_decode_prop",
+    "santa_decode_prop_strat",
+    "santa_decode_prop_iid",
     "santa_decode_flash",
     "exact_decode",
     "santa_read_device_error",
@@ -86,7 +88,7 @@ def lib() -> ctypes.CDLL:
         vp, sz = ctypes.c_void_p, ctypes.c_size_t
         P, Dp = ctypes.POINTER(Problem), ctypes.POINTER(Debug)
         L.santa_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
-        for name in ("santa_decode_prop", "santa_decode_flash"):
+        for name in ("santa_decode_prop", "santa_decode_prop_strat", "santa_decode_prop_iid", "santa_decode_flash"):
             getattr(L, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.exact_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_decode_prop_static_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, Dp, vp]
@@ -147,6 +149,18 @@ def santa_decode_prop(problem, q, k, v, kv_indptr, U, out, workspace, debug=None
           workspace, debug, stream)
 
 
+def santa_decode_prop_strat(problem, q, k, v, kv_indptr, u, out, workspace, debug=None, stream=None):
+    """S2ANTA-strat through the prop pipeline: u is [B][Hq][S] float32 in [0, 1)."""
+    _call("santa_decode_prop_strat", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(u), _ptr(out)],
+          workspace, debug, stream)
+
+
+def santa_decode_prop_iid(problem, q, k, v, kv_indptr, u, out, workspace, debug=None, stream=None):
+    """SANTA (i.i.d. draws) through the prop pipeline: u is [B][Hq][S] float32 in [0, 1)."""
+    _call("santa_decode_prop_iid", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(u), _ptr(out)],
+          workspace, debug, stream)
+
+
 def santa_decode_flash(problem, q, k, v, kv_indptr, U, out, workspace, debug=None, stream=None):
     """S2ANTA-flash decode: see santa_decode.h."""
     _call("santa_decode_flash", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(U), _ptr(out)],
@@ -181,13 +195,18 @@ def santa_read_device_error(error_flags, stream=None) -> int:
     return h.value
 
 
-MODES = {"prop": MODE_PROP, "flash": MODE_FLASH, "exact": MODE_EXACT}
+MODES = {"prop": MODE_PROP, "strat": MODE_PROP, "iid": MODE_PROP, "flash": MODE_FLASH, "exact": MODE_EXACT}
 
 
 def decode(mode: str, problem, q, k, v, kv_indptr, U, out, workspace, debug=None, stream=None):
-    """Dispatch by mode name ('prop', 'flash', 'exact'; U is ignored by 'exact')."""
+    """Dispatch by mode name ('prop', 'strat', 'iid', 'flash', 'exact'); U is the offsets
+    [B][Hq] for prop and flash, the uniforms [B][Hq][S] for strat and iid, ignored by exact."""
     if mode == "prop":
         santa_decode_prop(problem, q, k, v, kv_indptr, U, out, workspace, debug, stream)
+    elif mode == "strat":
+        santa_decode_prop_strat(problem, q, k, v, kv_indptr, U, out, workspace, debug, stream)
+    elif mode == "iid":
+        santa_decode_prop_iid(problem, q, k, v, kv_indptr, U, out, workspace, debug, stream)
     elif mode == "flash":
         santa_decode_flash(problem, q, k, v, kv_indptr, U, out, workspace, debug, stream)
     elif mode == "exact":

@@ -85,7 +85,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     return SANTA_OK;
 }
 
-int smem_check(const santa_problem *p, int mode) {
+int smem_check(const santa_problem *p, int mode, int sampler) {
     constexpr size_t kOptin = 227 * 1024;  // shared memory a block may opt in to on sm_103
     const int G = p->num_q_heads / p->num_kv_heads;
     size_t need = 0;
@@ -93,7 +93,7 @@ int smem_check(const santa_problem *p, int mode) {
         Layout L;
         if (make_layout(p, mode, &L) != SANTA_OK) return SANTA_INVALID_ARG;
         need = prop_pass1_smem(p->dtype, p->head_dim, G, int(kOptin));
-        const size_t s2 = prop_pass2_smem(p->head_dim, L.cps);
+        const size_t s2 = prop_pass2_smem(p->head_dim, L.cps, sampler, p->S);
         if (s2 > need) need = s2;
     } else if (mode == SANTA_MODE_FLASH) {
         need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
@@ -165,11 +165,13 @@ bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long 
     return true;
 }
 
-int run(int mode, const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
-        const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
-        santa_stream_t stream_) {
+// `sampler` (prop only): kSys with offsets U [B][Hq], or kStrat / kIid with uniforms U [B][Hq][S].
+int run(int mode, int sampler, const santa_problem *p, const void *q, const void *k, const void *v,
+        const long long *kv_indptr, const float *U, float *out, void *workspace, size_t workspace_bytes,
+        const santa_debug *dbg, santa_stream_t stream_) {
     int st = check_problem(p, mode);
     if (st != SANTA_OK) return st;
+    if (sampler != kSys && p->S > kMaxSamplerS) return SANTA_UNSUPPORTED;
     if (p->batch == 0) return SANTA_OK;
     if (!q || !k || !v || !kv_indptr || !out || !workspace) return SANTA_INVALID_ARG;
     if (mode != SANTA_MODE_EXACT && !U) return SANTA_INVALID_ARG;
@@ -181,7 +183,7 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     st = make_layout(p, mode, &L);
     if (st != SANTA_OK) return st;
     if (workspace_bytes < L.total) return SANTA_WORKSPACE_TOO_SMALL;
-    st = smem_check(p, mode);
+    st = smem_check(p, mode, sampler);
     if (st != SANTA_OK) return st;
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -210,7 +212,9 @@ int run(int mode, const santa_problem *p, const void *q, const void *k, const vo
     prm.k = k;
     prm.v = v;
     prm.kv_indptr = kv_indptr;
-    prm.U = U;
+    prm.U = sampler == kSys ? U : nullptr;
+    prm.u_samples = sampler == kSys ? nullptr : U;
+    prm.sampler = sampler;
     prm.out = out;
     prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
     prm.rec_z = reinterpret_cast<float *>(ws + L.rec_z);
@@ -269,18 +273,30 @@ int santa_workspace_size(const santa_problem *p, int mode, size_t *bytes) {
 int santa_decode_prop(const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
                       const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
                       santa_stream_t stream) {
-    return run(SANTA_MODE_PROP, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
+    return run(SANTA_MODE_PROP, kSys, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
+}
+
+int santa_decode_prop_strat(const santa_problem *p, const void *q, const void *k, const void *v,
+                            const long long *kv_indptr, const float *u, float *out, void *workspace,
+                            size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
+    return run(SANTA_MODE_PROP, kStrat, p, q, k, v, kv_indptr, u, out, workspace, workspace_bytes, dbg, stream);
+}
+
+int santa_decode_prop_iid(const santa_problem *p, const void *q, const void *k, const void *v,
+                          const long long *kv_indptr, const float *u, float *out, void *workspace,
+                          size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
+    return run(SANTA_MODE_PROP, kIid, p, q, k, v, kv_indptr, u, out, workspace, workspace_bytes, dbg, stream);
 }
 
 int santa_decode_flash(const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
                        const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
                        santa_stream_t stream) {
-    return run(SANTA_MODE_FLASH, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
+    return run(SANTA_MODE_FLASH, kSys, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
 }
 
 int exact_decode(const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,
                  float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
-    return run(SANTA_MODE_EXACT, p, q, k, v, kv_indptr, nullptr, out, workspace, workspace_bytes, dbg, stream);
+    return run(SANTA_MODE_EXACT, kSys, p, q, k, v, kv_indptr, nullptr, out, workspace, workspace_bytes, dbg, stream);
 }
 
 int santa_read_device_error(unsigned int *error_flags, santa_stream_t stream_, unsigned int *flags) {

@@ -22,6 +22,11 @@ constexpr int kMergeThreads = 128;
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
 
 enum Mode { kProp = 0, kFlash = 1, kExact = 2 };
+// Thresholds of the prop sampler ("Stochastic Sparse Attention for Memory-Bound
+// Inference", paper notes, Key design 1): systematic U + m/S, stratified
+// (m + u_m)/S, or i.i.d. u_s (taken in increasing order).
+enum Sampler { kSys = 0, kStrat = 1, kIid = 2 };
+constexpr int kMaxSamplerS = 16384;  // stratified / i.i.d.: the head's S uniforms sit in shared memory
 
 // Everything a kernel needs; built by the host entry points.
 struct Params {
@@ -31,7 +36,8 @@ struct Params {
     float scale;  // 1/sqrt(d)
     const void *q, *k, *v;
     const long long *kv_indptr;
-    const float *U;
+    const float *U;          // prop (systematic) / flash: offsets [B][Hq] in [0, 1/S)
+    const float *u_samples;  // prop stratified / i.i.d.: uniforms [B][Hq][S] in [0, 1)
     float *out;
     // workspace
     float *rec_m, *rec_z;  // flash/exact: [B][Hq][Tmax] tile max logit and partition sum;
@@ -39,6 +45,7 @@ struct Params {
     float *stash;          // prop: [Hq][total_tokens] exp(x - m_c)
     float *partial;        // flash/exact: [B][Hq][Tmax][D] tile estimates
     int nsplit, chunks_per_split;  // prop pass 2: CTAs (one cluster) per head, chunks per CTA
+    int sampler;                   // prop: kSys, kStrat or kIid
     // optional debug outputs
     float *dbg_tile_m, *dbg_tile_z;
     int *dbg_count, *dbg_idx;

@@ -23,7 +23,8 @@
 // batch, maps it to its chunk's own scale,
 //     r_m = ((U + m/S) Z - C_{c-1}) / exp(m_c - M),
 // takes the smallest key whose prefix exceeds r_m (clamped to the chunk's keys
-// of positive score), and queues that key; the queue is flushed by gathering
+// of positive score), and queues that key (the stratified and i.i.d. samplers of
+// Key design 1 only change the thresholds: (m + u_m)/S, or the sorted u_s); the queue is flushed by gathering
 // up to 32 V rows at a time.  Each CTA sums its warps in warp order and stores
 // the sum into the shared memory of cluster rank 0, which adds the CTAs in
 // rank order after one cluster barrier.  out = sum / S: no multiply by a
@@ -132,10 +133,40 @@ struct Pass2Smem {
     static __host__ __device__ size_t wl_off(int cps) { return last_off(cps) + size_t(kPass2Warps) * kP2Batch * 4; }
     static __host__ __device__ size_t red_off(int cps) { return wl_off(cps) + size_t(kPass2Warps) * 32 * 4; }
     static __host__ __device__ size_t part_off(int cps) { return red_off(cps) + size_t(kPass2Warps) * D * 4; }
-    static __host__ __device__ size_t bytes(int cps) { return part_off(cps) + size_t(kMaxSplit) * D * 4; }
+    static __host__ __device__ size_t u_off(int cps) { return part_off(cps) + size_t(kMaxSplit) * D * 4; }
+    // nu: the head's uniforms (stratified / i.i.d. samplers), padded to a power of two; 0 otherwise
+    static __host__ __device__ size_t bytes(int cps, int nu) { return u_off(cps) + size_t(nu) * 4; }
 };
 
-template <typename T, int D>
+// Uniforms of a stratified / i.i.d. prop call: S rounded up to a power of two (the
+// i.i.d. sampler sorts them), 0 for the systematic sampler.
+__host__ __device__ inline int sampler_slots(int sampler, int S) {
+    if (sampler == kSys) return 0;
+    int n = 1;
+    while (n < S) n <<= 1;
+    return n;
+}
+
+// Ascending bitonic sort of a[0, n) in shared memory by the whole block (n a power of two).
+template <int NT>
+__device__ __forceinline__ void block_bitonic_sort(float *a, int n) {
+    for (int k = 2; k <= n; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += NT) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const float x = a[i], y = a[ixj];
+                    if ((x > y) == ((i & k) == 0)) {
+                        a[i] = y;
+                        a[ixj] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+}
+
+template <typename T, int D, int SAMPLER>
 __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const Params p) {
     constexpr int kThreads = kPass2Warps * 32;
     constexpr int kE = D / 32;
@@ -158,14 +189,34 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     int *wl = reinterpret_cast<int *>(smem + Lay::wl_off(cps)) + warp * 32;
     float *red = reinterpret_cast<float *>(smem + Lay::red_off(cps));
     float *part = reinterpret_cast<float *>(smem + Lay::part_off(cps));
+    float *s_u = reinterpret_cast<float *>(smem + Lay::u_off(cps));  // stratified / i.i.d. uniforms
 
     pdl_launch_dependents();  // the next call's pass 1 may start its prologue on free SMs
     cluster_arrive();         // first half of the barrier that makes every CTA's shared memory addressable
 
-    // Inputs the previous kernel does not write may be read before the dependency wait.
+    // Inputs the previous kernel does not write may be read before the dependency wait
+    // (pass 1 lets this kernel start only once its own predecessor is complete).
     long long start;
     const int L = seq_bounds(p, b, &start);
-    const float u = load_offset(p, b, hq);
+    const float u = SAMPLER == kSys ? load_offset(p, b, hq) : 0.f;
+    if constexpr (SAMPLER != kSys) {
+        // the head's S uniforms, each checked into [0, 1); the i.i.d. ones sorted
+        const int nu = sampler_slots(SAMPLER, p.S);
+        const float *ug = p.u_samples + (size_t(b) * p.Hq + hq) * p.S;
+        for (int i = tid; i < nu; i += kThreads) {
+            float x = INFINITY;  // padding sorts last
+            if (i < p.S) {
+                x = __ldg(ug + i);
+                if (!(x >= 0.f && x < 1.f)) {
+                    raise_flag(p, SANTA_ERR_OFFSET);
+                    x = x >= 1.f ? nextafterf(1.f, 0.f) : 0.f;
+                }
+            }
+            s_u[i] = x;
+        }
+        __syncthreads();
+        if constexpr (SAMPLER == kIid) block_bitonic_sort<kThreads>(s_u, nu);
+    }
     pdl_wait();
 
     const int Nb = (L + kChunkRows - 1) / kChunkRows;
@@ -254,8 +305,28 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
         if (c_lo == 0 && tid == 0) sC[0] = 0ull;
         __syncthreads();
 
-        // threshold counts: N(C_{c-1}) for c = c_lo .. c_hi (monotone in C)
+        // threshold counts: N(C_{c-1}) for c = c_lo .. c_hi, the number of thresholds
+        // below the normalised CDF value cn = C / Z (each form is monotone in cn)
         const float Sf = float(p.S), SU = Sf * u, fZ = __ull2float_rn(Z);
+        auto thresholds_below = [&](float cn) -> int {
+            if constexpr (SAMPLER == kSys) {  // U + m/S < cn  <=>  m < S cn - S U
+                return int(fminf(fmaxf(ceilf(fmaf(Sf, cn, -SU)), 0.f), Sf));
+            } else if constexpr (SAMPLER == kStrat) {  // (m + u_m)/S < cn: all m < floor(S cn), maybe one more
+                const float y = Sf * cn;
+                const int k = int(fminf(fmaxf(floorf(y), 0.f), Sf));
+                return k + ((k < p.S && s_u[k] < y - float(k)) ? 1 : 0);
+            } else {  // sorted u_s < cn
+                int lo = 0, hi = p.S;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_u[mid] < cn)
+                        lo = mid + 1;
+                    else
+                        hi = mid;
+                }
+                return lo;
+            }
+        };
         for (int i = tid; i <= c_hi - c_lo; i += kThreads) {
             const int c = c_lo + i - 1;
             int n;
@@ -264,7 +335,7 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
             else if (c == Nb - 1)
                 n = p.S;
             else
-                n = int(fminf(fmaxf(ceilf(fmaf(Sf, __ull2float_rn(sC[i]) / fZ, -SU)), 0.f), Sf));
+                n = thresholds_below(__ull2float_rn(sC[i]) / fZ);
             sN[i] = n;
         }
         __syncthreads();
@@ -348,7 +419,13 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
                         if (wcum[k + s - 1] <= g) k += s;
                     const int c = c0 + k, i = c - c_lo;
                     const int m = sN[i] + g - (k > 0 ? wcum[k - 1] : 0);
-                    const float thr = fmaf(float(m), invS, u);
+                    float thr;  // threshold m of the sampler
+                    if constexpr (SAMPLER == kSys)
+                        thr = fmaf(float(m), invS, u);
+                    else if constexpr (SAMPLER == kStrat)
+                        thr = (float(m) + s_u[m]) * invS;
+                    else
+                        thr = s_u[m];
                     const float r = fmaf(thr, Zf, -__ull2float_rn(sC[i]) / kMassScale) / s_st[i];
                     const int len = min(kChunkRows, L - c * kChunkRows);
                     const int j = c * kChunkRows + cdf_search(wev + k * 32, len, r, wlast[k]);

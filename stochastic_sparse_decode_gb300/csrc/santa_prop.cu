@@ -18,8 +18,19 @@ size_t prop_pass1_smem(int dtype, int d, int g, int smem_optin) {
     return bytes;
 }
 
-size_t prop_pass2_smem(int d, int cps) {
-    return d == 128 ? Pass2Smem<uint16_t, 128>::bytes(cps) : Pass2Smem<uint16_t, 64>::bytes(cps);
+size_t prop_pass2_smem(int d, int cps, int sampler, int S) {
+    const int nu = sampler_slots(sampler, S);
+    return d == 128 ? Pass2Smem<uint16_t, 128>::bytes(cps, nu) : Pass2Smem<uint16_t, 64>::bytes(cps, nu);
+}
+
+template <typename T, int D>
+static void *pass2_for(int sampler) {
+    switch (sampler) {
+        case kSys: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys>);
+        case kStrat: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kStrat>);
+        case kIid: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kIid>);
+        default: return nullptr;
+    }
 }
 
 // SM count and opt-in shared memory per block of the current device (cached).
@@ -52,8 +63,9 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
         if (!nbuf) return cudaErrorNotSupported;
         auto k1 = prop_stream_kernel<T, D, G>;
         const size_t s1 = CG::bytes(nbuf);
-        auto k2 = prop_pass2_kernel<T, D>;
-        const size_t s2 = Pass2Smem<T, D>::bytes(p.chunks_per_split);
+        auto k2 = reinterpret_cast<void (*)(const Params)>(pass2_for<T, D>(p.sampler));
+        if (!k2) return cudaErrorInvalidValue;
+        const size_t s2 = Pass2Smem<T, D>::bytes(p.chunks_per_split, sampler_slots(p.sampler, p.S));
         cudaError_t e = ensure_smem(k1, s1);
         if (e == cudaSuccess) e = ensure_smem(k2, s2);
         if (e != cudaSuccess) return e;

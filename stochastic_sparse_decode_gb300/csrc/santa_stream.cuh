@@ -150,7 +150,6 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     ChunkSlot *slots = reinterpret_cast<ChunkSlot *>(smem + CG::slots_off(nbuf)) + warp * kChunkMaxBuf;
     int *s_next = reinterpret_cast<int *>(smem + CG::next_off(nbuf));
 
-    pdl_launch_dependents();
     if (lane < nbuf) mbar_init(&bars[lane], 1);
     if (threadIdx.x == 0) {
         *s_next = 0;
@@ -161,6 +160,9 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     // Nothing above touches global memory; the previous kernel in the stream (which
     // may produce q, K or read this call's workspace) must be complete below.
     pdl_wait();
+    // Only now may pass 2 start: it reads the call's inputs before its own
+    // dependency wait, and they are final once the kernel before this one is.
+    pdl_launch_dependents();
 
     // lane 0's cache of the last sequence's bounds
     int lb = -1, lL = 0;

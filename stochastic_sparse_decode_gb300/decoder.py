@@ -42,7 +42,7 @@ class Decoder:
             "tile_count": torch.full((B, Hq, T), -1, dtype=torch.int32, device=dev),
             "error_flags": torch.zeros(1, dtype=torch.int32, device=dev),
         }
-        if mode == "prop":
+        if mode in ("prop", "strat", "iid"):
             bufs["sample_idx"] = torch.full((B, Hq, p.S), -1, dtype=torch.int32, device=dev)
         elif mode == "flash":
             bufs["sample_idx"] = torch.full((B, Hq, T, max(sample_stride, 1)), -1, dtype=torch.int32, device=dev)

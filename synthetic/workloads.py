@@ -200,6 +200,14 @@ def draw_offsets(S: int, shape, rng: np.random.Generator) -> np.ndarray:
     return U
 
 
+def draw_uniforms(shape, rng: np.random.Generator) -> np.ndarray:
+    """Uniforms in [0, 1) as float32 values strictly below 1 (the stratified and
+    i.i.d. samplers' draws, passed to both sides as inputs)."""
+    u = rng.random(size=shape, dtype=np.float64).astype(np.float32)
+    u[u >= np.float32(1.0)] = np.nextafter(np.float32(1.0), np.float32(0.0), dtype=np.float32)
+    return u
+
+
 def generate(w: Workload, instance: int = 0, n_offsets: int | None = None) -> Inputs:
     """Draw one seeded instance of workload ``w``."""
     seed = 1000 * w.config + instance

@@ -82,6 +82,9 @@ def check(inp: Inputs, mode: str, res: dict, S: int | None = None, U_index: int 
             rep.merge(compare.check_prop_head(q, K, V, S, float(U[b, h]), w.tile, res["out"][b, h],
                                               res["sample_idx"][b, h], res["tile_count"][b, h],
                                               res["tile_m"][b, h], res["tile_z"][b, h], what=what))
+        elif mode in ("strat", "iid"):
+            rep.merge(compare.check_sampled_head(mode, q, K, V, U[b, h], res["out"][b, h], res["sample_idx"][b, h],
+                                                 what=what))
         elif mode == "flash":
             rep.merge(compare.check_flash_head(q, K, V, S, float(U[b, h]), w.tile, res["out"][b, h],
                                                res["sample_idx"][b, h], res["tile_m"][b, h],

@@ -157,6 +157,24 @@ def test_null_misaligned_and_small_workspace_are_rejected(sd):
     assert _call_prop(sd, _north_star(sd, batch=0), q=None, k=None) == sd.OK
 
 
+@pytest.mark.parametrize("name", ["santa_decode_prop_strat", "santa_decode_prop_iid"])
+def test_sampler_modes_refuse_more_uniforms_than_shared_memory_holds(sd, name):
+    """The stratified and i.i.d. samplers keep a head's S uniforms on chip: S <= 16384."""
+    t = _FakeTensor
+    for S, status in ((16385, sd.UNSUPPORTED), (1 << 20, sd.UNSUPPORTED)):
+        p = _north_star(sd, S=S)
+        ws = sd.workspace_size(p, sd.MODE_PROP)
+        with pytest.raises(sd.SantaError) as e:
+            getattr(sd, name)(p, t(0x10000), t(0x20000), t(0x30000), t(0x40000), t(0x50000), t(0x60000),
+                              t(0x100000, ws), stream=0)
+        assert e.value.status == status
+    p = _north_star(sd, S=64)
+    with pytest.raises(sd.SantaError) as e:  # null uniforms
+        getattr(sd, name)(p, t(0x10000), t(0x20000), t(0x30000), t(0x40000), None, t(0x60000),
+                          t(0x100000, sd.workspace_size(p, sd.MODE_PROP)), stream=0)
+    assert e.value.status == sd.INVALID_ARG
+
+
 def test_exact_needs_no_offsets(sd):
     p = _north_star(sd)
     ws = sd.workspace_size(p, sd.MODE_EXACT)
