@@ -138,13 +138,33 @@ struct Pass2Smem {
     static __host__ __device__ size_t bytes(int cps, int nu) { return u_off(cps) + size_t(nu) * 4; }
 };
 
-// Uniforms of a stratified / i.i.d. prop call: S rounded up to a power of two (the
-// i.i.d. sampler sorts them), 0 for the systematic sampler.
+constexpr int kRankSortMax = 512;  // i.i.d. uniforms up to this many are sorted by rank
+
+// Shared-memory floats for the uniforms of a stratified / i.i.d. prop call: S
+// rounded up to a power of two (the i.i.d. sampler sorts them; a rank sort needs
+// a second array), 0 for the systematic sampler.
 __host__ __device__ inline int sampler_slots(int sampler, int S) {
     if (sampler == kSys) return 0;
     int n = 1;
     while (n < S) n <<= 1;
-    return n;
+    return (sampler == kIid && n <= kRankSortMax) ? 2 * n : n;
+}
+
+// Ascending sort of a[0, n) into out[0, n) by rank, in one pass: element i goes to
+// #{k : a[k] < a[i]} + #{k < i : a[k] == a[i]}, a distinct slot for every i.  Ends
+// with a block barrier.
+template <int NT>
+__device__ __forceinline__ void block_rank_sort(const float *a, float *out, int n) {
+    for (int i = threadIdx.x; i < n; i += NT) {
+        const float x = a[i];
+        int r = 0;
+        for (int k = 0; k < n; ++k) {
+            const float y = a[k];
+            r += (y < x || (y == x && k < i)) ? 1 : 0;
+        }
+        out[r] = x;
+    }
+    __syncthreads();
 }
 
 // Ascending bitonic sort of a[0, n) in shared memory by the whole block (n a power of two).
@@ -201,7 +221,8 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     const float u = SAMPLER == kSys ? load_offset(p, b, hq) : 0.f;
     if constexpr (SAMPLER != kSys) {
         // the head's S uniforms, each checked into [0, 1); the i.i.d. ones sorted
-        const int nu = sampler_slots(SAMPLER, p.S);
+        int nu = 1;
+        while (nu < p.S) nu <<= 1;
         const float *ug = p.u_samples + (size_t(b) * p.Hq + hq) * p.S;
         for (int i = tid; i < nu; i += kThreads) {
             float x = INFINITY;  // padding sorts last
@@ -215,7 +236,14 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
             s_u[i] = x;
         }
         __syncthreads();
-        if constexpr (SAMPLER == kIid) block_bitonic_sort<kThreads>(s_u, nu);
+        if constexpr (SAMPLER == kIid) {
+            if (nu <= kRankSortMax) {
+                block_rank_sort<kThreads>(s_u, s_u + nu, nu);
+                s_u += nu;  // the sorted copy
+            } else {
+                block_bitonic_sort<kThreads>(s_u, nu);
+            }
+        }
     }
     pdl_wait();
 
