@@ -297,6 +297,30 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
 #pragma unroll
         for (int w = 1; w < kPass2Warps; ++w) M = fmaxf(M, scrf[w]);
 
+        // threshold counts N(c): the number of the sampler's thresholds below the
+        // normalised CDF value cn = C / Z (each form is monotone in cn)
+        const float Sf = float(p.S), SU = Sf * u;
+        auto thresholds_below = [&](float cn) -> int {
+            if constexpr (SAMPLER == kSys) {  // U + m/S < cn  <=>  m < S cn - S U
+                return int(fminf(fmaxf(ceilf(fmaf(Sf, cn, -SU)), 0.f), Sf));
+            } else if constexpr (SAMPLER == kStrat) {  // (m + u_m)/S < cn: all m < floor(S cn), maybe one more
+                const float y = Sf * cn;
+                const int k = int(fminf(fmaxf(floorf(y), 0.f), Sf));
+                return k + ((k < p.S && s_u[k] < y - float(k)) ? 1 : 0);
+            } else {  // sorted u_s < cn
+                int lo = 0, hi = p.S;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_u[mid] < cn)
+                        lo = mid + 1;
+                    else
+                        hi = mid;
+                }
+                return lo;
+            }
+        };
+        // C (and, when the head's records fit one block, N at once: Z is that block's sum)
+        const bool one_block = Nb <= kBlk;
         u64 carry = 0;
         for (int base = 0, it = 0; base < Nb; base += kBlk, ++it) {
             if (base > 0) load_block(base);
@@ -322,51 +346,39 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
                 btot += t;
             }
             const u64 excl = carry + woff + (incl - run);
+            const float fZb = __ull2float_rn(btot);
 #pragma unroll
             for (int k = 0; k < kP2Rec; ++k) {
                 const int c = base + tid * kP2Rec + k;
-                if (c >= c_lo - 1 && c < c_hi) sC[c - c_lo + 1] = excl + pl[k];
+                if (c >= c_lo - 1 && c < c_hi) {
+                    const u64 Cc = excl + pl[k];
+                    sC[c - c_lo + 1] = Cc;
+                    if (one_block) sN[c - c_lo + 1] = c == Nb - 1 ? p.S : thresholds_below(__ull2float_rn(Cc) / fZb);
+                }
             }
             carry += btot;
         }
         const u64 Z = carry;  // = C_{N_b - 1}
-        if (c_lo == 0 && tid == 0) sC[0] = 0ull;
-        __syncthreads();
-
-        // threshold counts: N(C_{c-1}) for c = c_lo .. c_hi, the number of thresholds
-        // below the normalised CDF value cn = C / Z (each form is monotone in cn)
-        const float Sf = float(p.S), SU = Sf * u, fZ = __ull2float_rn(Z);
-        auto thresholds_below = [&](float cn) -> int {
-            if constexpr (SAMPLER == kSys) {  // U + m/S < cn  <=>  m < S cn - S U
-                return int(fminf(fmaxf(ceilf(fmaf(Sf, cn, -SU)), 0.f), Sf));
-            } else if constexpr (SAMPLER == kStrat) {  // (m + u_m)/S < cn: all m < floor(S cn), maybe one more
-                const float y = Sf * cn;
-                const int k = int(fminf(fmaxf(floorf(y), 0.f), Sf));
-                return k + ((k < p.S && s_u[k] < y - float(k)) ? 1 : 0);
-            } else {  // sorted u_s < cn
-                int lo = 0, hi = p.S;
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (s_u[mid] < cn)
-                        lo = mid + 1;
-                    else
-                        hi = mid;
-                }
-                return lo;
-            }
-        };
-        for (int i = tid; i <= c_hi - c_lo; i += kThreads) {
-            const int c = c_lo + i - 1;
-            int n;
-            if (c < 0)
-                n = 0;
-            else if (c == Nb - 1)
-                n = p.S;
-            else
-                n = thresholds_below(__ull2float_rn(sC[i]) / fZ);
-            sN[i] = n;
+        if (c_lo == 0 && tid == 0) {
+            sC[0] = 0ull;
+            sN[0] = 0;
         }
         __syncthreads();
+        const float fZ = __ull2float_rn(Z);
+        if (!one_block) {  // N(C_{c-1}) for c = c_lo .. c_hi
+            for (int i = tid; i <= c_hi - c_lo; i += kThreads) {
+                const int c = c_lo + i - 1;
+                int n;
+                if (c < 0)
+                    n = 0;
+                else if (c == Nb - 1)
+                    n = p.S;
+                else
+                    n = thresholds_below(__ull2float_rn(sC[i]) / fZ);
+                sN[i] = n;
+            }
+            __syncthreads();
+        }
 
         // ---- debug: per tile of this CTA, m_t, Z_tile (on the m_t scale) and S_tile
         if (p.dbg_tile_m || p.dbg_tile_z || p.dbg_count) {
