@@ -141,7 +141,7 @@ int santa_workspace_size(const santa_problem *p, int mode, size_t *bytes);
  * and pass 2 (reducer over the ceil(L_b / 32) chunk records, per-chunk
  * systematic search, V gather, deterministic combine).  Workspace: the chunk
  * records, 2 x [B][Hq][ceil(max_len / 32)] float32, and the score stash
- * [Hq][total_tokens] float32.  Supported up to max_len of about 4 million keys
+ * [B][Hq][max_len] float32.  Supported up to max_len of about 4 million keys
  * (pass 2 keeps its share of the chunk records in shared memory; longer is
  * SANTA_UNSUPPORTED).  Returns a status; see the conventions above.
  */
@@ -208,7 +208,7 @@ int exact_decode(const santa_problem *p, const void *q, const void *k, const voi
  * that every GPU loading this library holds until the process exits.  Problems
  * whose prop workspace (santa_workspace_size with SANTA_MODE_PROP) exceeds that
  * size are rejected with SANTA_WORKSPACE_TOO_SMALL before anything is enqueued;
- * roughly, num_q_heads * total_tokens must stay below about 4 million.  The other
+ * roughly, batch * num_q_heads * max_len must stay below about 4 million.  The other
  * arguments, their layouts, ownership and errors are those of santa_decode_prop.
  * Nothing is allocated: not by this call, and not by any routine it calls.
  *

@@ -50,7 +50,7 @@ int check_problem(const santa_problem *p, int mode) {
 // Workspace regions of one call, each 256-byte aligned.  Sizes are computed in
 // double first so that absurd shapes are rejected instead of wrapping around.
 //   prop:        chunk records rec_m, rec_z [B][Hq][nch], nch = ceil(max_len / 32),
-//                and the score stash [Hq][total_tokens];
+//                and the score stash [B][Hq][max_len];
 //   flash/exact: tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d].
 int make_layout(const santa_problem *p, int mode, Layout *L) {
     const int Tmax = (p->max_len + p->tile - 1) / p->tile;
@@ -60,7 +60,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     const double nrec = B * Hq * (prop ? nch : Tmax);
     double est = 2 * nrec * 4;
     if (prop)
-        est += Hq * double(p->total_tokens) * 4;
+        est += B * Hq * double(p->max_len) * 4;
     else
         est += nrec * D * 4;
     if (est > 1e15) return SANTA_INVALID_ARG;
@@ -76,7 +76,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     off += align256(n_rec * 4);
     if (prop) {
         L->stash = off;
-        off += align256(size_t(p->num_q_heads) * size_t(p->total_tokens) * 4);
+        off += align256(size_t(p->batch) * p->num_q_heads * size_t(p->max_len) * 4);
     } else {
         L->partial = off;
         off += align256(n_rec * p->head_dim * 4);

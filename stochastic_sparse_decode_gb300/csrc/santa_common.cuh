@@ -42,7 +42,7 @@ struct Params {
     // workspace
     float *rec_m, *rec_z;  // flash/exact: [B][Hq][Tmax] tile max logit and partition sum;
                            // prop: [B][Hq][nch] the same per 32-key chunk
-    float *stash;          // prop: [Hq][total_tokens] exp(x - m_c)
+    float *stash;          // prop: [B][Hq][max_len] exp(x - m_c), key i of sequence b at i
     float *partial;        // flash/exact: [B][Hq][Tmax][D] tile estimates
     int nsplit, chunks_per_split;  // prop pass 2: CTAs (one cluster) per head, chunks per CTA
     int sampler;                   // prop: kSys, kStrat or kIid

@@ -214,6 +214,31 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     pdl_launch_dependents();  // the next call's pass 1 may start its prologue on free SMs
     cluster_arrive();         // first half of the barrier that makes every CTA's shared memory addressable
 
+    // One round trip for everything the reducer and the first batch need: the first
+    // block of chunk records, speculatively the stash of this warp's first 16 chunks
+    // (the stash is laid out per (sequence, head) with a stride of max_len, so no
+    // address waits for another load), the sequence bounds and the offset.  Values
+    // past the sequence's end are masked once its length is known.
+    const size_t rec0 = (size_t(b) * p.Hq + hq) * p.nch;
+    const float *sseq = p.stash + (size_t(b) * p.Hq + hq) * p.max_len;
+    const int cw0 = split * cps + warp * kper;  // this warp's first chunk
+    float mr[kP2Rec], zr[kP2Rec];
+    auto load_block = [&](int base, int lim) {
+#pragma unroll
+        for (int k = 0; k < kP2Rec; ++k) {
+            const int c = base + tid * kP2Rec + k;
+            mr[k] = c < lim ? __ldcg(p.rec_m + rec0 + c) : -INFINITY;
+            zr[k] = c < lim ? __ldcg(p.rec_z + rec0 + c) : 0.f;
+        }
+    };
+    load_block(0, p.nch);
+    float ev[kP2Batch];
+#pragma unroll
+    for (int k = 0; k < kP2Batch; ++k) {
+        const int c = cw0 + k;
+        const int key = c * kChunkRows + lane;
+        ev[k] = (k < kper && key < p.max_len) ? __ldcg(sseq + key) : 0.f;
+    }
     // Inputs the previous kernel does not write may be read before the dependency wait
     // (pass 1 lets this kernel start only once its own predecessor is complete).
     long long start;
@@ -250,37 +275,24 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     const int Nb = (L + kChunkRows - 1) / kChunkRows;
     const int c_lo = split * cps, c_hi = min(Nb, c_lo + cps);
     const bool active = c_lo < c_hi;  // CTA-uniform: this CTA owns at least one chunk
-    const int cw0 = c_lo + warp * kper, cw1 = min(c_hi, cw0 + kper);  // this warp's chunks
-    const size_t rec0 = (size_t(b) * p.Hq + hq) * p.nch;
-    const float *sseq = p.stash + size_t(hq) * p.total_tokens + start;
+    const int cw1 = min(c_hi, cw0 + kper);  // end of this warp's chunks
 
     float acc[kE];
 #pragma unroll
     for (int e = 0; e < kE; ++e) acc[e] = 0.f;
 
     if (active) {
-        // ---- one round trip: the first block of chunk records and, speculatively,
-        // the stash of this warp's first batch of chunks
-        float mr[kP2Rec], zr[kP2Rec];
-        auto load_block = [&](int base) {
+        // ---- mask what the speculative loads read past the sequence's end
 #pragma unroll
-            for (int k = 0; k < kP2Rec; ++k) {
-                const int c = base + tid * kP2Rec + k;
-                mr[k] = c < Nb ? __ldcg(p.rec_m + rec0 + c) : -INFINITY;
-                zr[k] = c < Nb ? __ldcg(p.rec_z + rec0 + c) : 0.f;
-            }
-        };
-        load_block(0);
-        {
-            float ev[kP2Batch];
-#pragma unroll
-            for (int k = 0; k < kP2Batch; ++k) {
-                const int c = cw0 + k;
-                const int key = c * kChunkRows + lane;
-                ev[k] = (c < cw1 && key < L) ? __ldcg(sseq + key) : 0.f;
+        for (int k = 0; k < kP2Rec; ++k)
+            if (tid * kP2Rec + k >= Nb) {
+                mr[k] = -INFINITY;
+                zr[k] = 0.f;
             }
 #pragma unroll
-            for (int k = 0; k < kP2Batch; ++k) wev[k * 32 + lane] = ev[k];
+        for (int k = 0; k < kP2Batch; ++k) {
+            const int c = cw0 + k;
+            wev[k * 32 + lane] = (c < cw1 && c * kChunkRows + lane < L) ? ev[k] : 0.f;
         }
 
         // ---- reducer: M; then C (fixed point, exact sums) and Z
@@ -323,13 +335,13 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
         const bool one_block = Nb <= kBlk;
         u64 carry = 0;
         for (int base = 0, it = 0; base < Nb; base += kBlk, ++it) {
-            if (base > 0) load_block(base);
+            if (base > 0) load_block(base, Nb);
             u64 pl[kP2Rec];  // this thread's chunks: local inclusive prefix
             u64 run = 0;
 #pragma unroll
             for (int k = 0; k < kP2Rec; ++k) {
                 const int c = base + tid * kP2Rec + k;
-                const float st = expf(mr[k] - M);
+                const float st = __expf(mr[k] - M);
                 if (c >= c_lo && c < c_hi) s_st[c - c_lo] = st;
                 run += c < Nb ? (u64)__float2ll_rn(zr[k] * st * kMassScale) : 0ull;
                 pl[k] = run;
@@ -346,14 +358,14 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
                 btot += t;
             }
             const u64 excl = carry + woff + (incl - run);
-            const float fZb = __ull2float_rn(btot);
+            const float rZb = 1.0f / __ull2float_rn(btot);
 #pragma unroll
             for (int k = 0; k < kP2Rec; ++k) {
                 const int c = base + tid * kP2Rec + k;
                 if (c >= c_lo - 1 && c < c_hi) {
                     const u64 Cc = excl + pl[k];
                     sC[c - c_lo + 1] = Cc;
-                    if (one_block) sN[c - c_lo + 1] = c == Nb - 1 ? p.S : thresholds_below(__ull2float_rn(Cc) / fZb);
+                    if (one_block) sN[c - c_lo + 1] = c == Nb - 1 ? p.S : thresholds_below(__ull2float_rn(Cc) * rZb);
                 }
             }
             carry += btot;

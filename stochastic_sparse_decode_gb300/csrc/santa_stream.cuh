@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
 #pragma unroll
             for (int bt = 1; bt < kGH; ++bt) m = fmaxf(m, x[bt]);
             m = head_max<kGH>(m);
-            float *srow = p.stash + size_t(hq) * p.total_tokens + row0;
+            float *srow = p.stash + (size_t(b) * p.Hq + hq) * p.max_len + size_t(ch) * kChunkRows;
             float z = 0.f;
 #pragma unroll
             for (int bt = 0; bt < kGH; ++bt) {

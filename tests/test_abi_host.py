@@ -60,8 +60,8 @@ def _north_star(sd, **kw):
 
 def test_workspace_layout_matches_the_byte_model(sd):
     """prop: 2 chunk-record arrays [B][Hq][ceil(max_len/32)] and the fp32 score
-    stash [Hq][n_k]; flash/exact: 2 tile-record arrays [B][Hq][T] and the tile
-    estimates [B][Hq][T][d]; each rounded up to 256 B."""
+    stash [B][Hq][max_len]; flash/exact: 2 tile-record arrays [B][Hq][T] and the
+    tile estimates [B][Hq][T][d]; each rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _north_star(sd)
     T, nch = 32768 // 256, 32768 // 32
@@ -74,7 +74,7 @@ def test_workspace_layout_matches_the_byte_model(sd):
     p = _north_star(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
     T, nch = 8, 32
     assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
-    assert sd.workspace_size(p, sd.MODE_PROP) == 2 * r(3 * 32 * nch * 4) + r(32 * 2000 * 4)
+    assert sd.workspace_size(p, sd.MODE_PROP) == 2 * r(3 * 32 * nch * 4) + r(3 * 32 * 1000 * 4)
 
 
 def test_very_long_prop_contexts_are_unsupported_not_wrong(sd):
