@@ -414,6 +414,12 @@ def run_ours(args, dist: Dist):
         exact_us = ms * 1000.0 / n_x
         extras["exact_us_per_layer_step"] = round(exact_us, 3)
         extras["speedup_vs_exact"] = round(exact_us / per_step_us, 3)
+        # how close the dense comparison kernel itself is to the HBM roofline (its
+        # algorithmic bytes: all of K and V, q, its tile records and estimates, out)
+        ex_bytes = byte_model(inp, "exact", w.S)["total"]
+        ex_gbs = ex_bytes / (exact_us * 1e-6) / 1e9
+        extras["exact_hbm_gbs"] = round(ex_gbs, 1)
+        extras["exact_roofline_frac"] = round(ex_gbs / measured_peaks()[0], 4)
         if w.name.startswith("llama8b"):
             wf = w.with_(S=2048)
             from synthetic.workloads import draw_offsets
