@@ -51,12 +51,30 @@ int check_problem(const santa_problem *p, int mode) {
 // double first so that absurd shapes are rejected instead of wrapping around.
 //   prop:        chunk records rec_m, rec_z [B][Hq][nch], nch = ceil(max_len / 32),
 //                and the score stash [B][Hq][max_len];
-//   flash/exact: tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d].
+//   flash:       tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d];
+//   exact:       per (sequence, streaming warp, head of the group) the partial state
+//                (M, Z) as rec_m [B][P][G][2] and O as [B][P][G][d], P the warps of
+//                the streaming kernel's largest grid.
 int make_layout(const santa_problem *p, int mode, Layout *L) {
     const int Tmax = (p->max_len + p->tile - 1) / p->tile;
     const int nch = (p->max_len + 31) / 32;
     const bool prop = mode == SANTA_MODE_PROP;
     const double B = p->batch, Hq = p->num_q_heads, D = p->head_dim;
+    if (mode == SANTA_MODE_EXACT) {
+        const int G = p->num_q_heads / p->num_kv_heads;
+        const int warps = exact_stream_warps(p->dtype, p->head_dim, G);
+        if (warps <= 0) return SANTA_UNSUPPORTED;
+        const double P = double(exact_stream_cta_bound(p->num_kv_heads)) * warps;
+        if (B * P * G * (D + 2) * 4 > 1e15) return SANTA_INVALID_ARG;
+        const size_t n = size_t(p->batch) * size_t(P) * G;
+        L->Tmax = Tmax;
+        L->nch = nch;
+        L->rec_m = 0;
+        L->rec_z = align256(n * 8);
+        L->partial = L->rec_z;
+        L->total = L->partial + align256(n * p->head_dim * 4);
+        return SANTA_OK;
+    }
     const double nrec = B * Hq * (prop ? nch : Tmax);
     double est = 2 * nrec * 4;
     if (prop)
@@ -98,7 +116,7 @@ int smem_check(const santa_problem *p, int mode, int sampler) {
     } else if (mode == SANTA_MODE_FLASH) {
         need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
     } else {
-        need = exact_tile_smem(p->dtype, p->head_dim, G, p->tile);
+        need = exact_stream_smem(p->dtype, p->head_dim, G);
     }
     return need <= kOptin ? SANTA_OK : SANTA_UNSUPPORTED;
 }
@@ -239,16 +257,15 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
     if (mode == SANTA_MODE_PROP) {
         if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32)) return SANTA_CUDA_ERROR;
         e = launch_prop(prm, p->dtype, kmap, stream, tm);
-    } else {
+    } else if (mode == SANTA_MODE_FLASH) {
         if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
             return SANTA_CUDA_ERROR;
-        if (mode == SANTA_MODE_FLASH) {
-            e = launch_flash(prm, p->dtype, kmap, stream, tm);
-        } else {
-            if (!kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
-                return SANTA_CUDA_ERROR;
-            e = launch_exact(prm, p->dtype, kmap, vmap, stream, tm);
-        }
+        e = launch_flash(prm, p->dtype, kmap, stream, tm);
+    } else {
+        if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32) ||
+            !kv_map(&vmap, v, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32))
+            return SANTA_CUDA_ERROR;
+        e = launch_exact(prm, p->dtype, kmap, vmap, stream, tm);
     }
     if (e == cudaErrorNotSupported) return SANTA_UNSUPPORTED;
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SANTA_CUDA_ERROR;

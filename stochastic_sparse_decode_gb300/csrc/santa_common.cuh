@@ -40,10 +40,12 @@ struct Params {
     const float *u_samples;  // prop stratified / i.i.d.: uniforms [B][Hq][S] in [0, 1)
     float *out;
     // workspace
-    float *rec_m, *rec_z;  // flash/exact: [B][Hq][Tmax] tile max logit and partition sum;
-                           // prop: [B][Hq][nch] the same per 32-key chunk
+    float *rec_m, *rec_z;  // flash: [B][Hq][Tmax] tile max logit and partition sum;
+                           // prop: [B][Hq][nch] the same per 32-key chunk;
+                           // exact: rec_m holds float2 (M, Z) per (sequence, warp, head)
     float *stash;          // prop: [B][Hq][max_len] exp(x - m_c), key i of sequence b at i
-    float *partial;        // flash/exact: [B][Hq][Tmax][D] tile estimates
+    float *partial;        // flash: [B][Hq][Tmax][D] tile estimates;
+                           // exact: [sequence slot][warp][head][D] unnormalised sums
     int nsplit, chunks_per_split;  // prop pass 2: CTAs (one cluster) per head, chunks per CTA
     int sampler;                   // prop: kSys, kStrat or kIid
     // optional debug outputs

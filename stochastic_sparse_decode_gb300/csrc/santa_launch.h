@@ -92,7 +92,18 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
 size_t prop_pass1_smem(int dtype, int D, int G, int smem_optin);
 size_t prop_pass2_smem(int D, int cps, int sampler, int S);
 size_t flash_tile_smem(int dtype, int D, int G, int tile);
-size_t exact_tile_smem(int dtype, int D, int G, int tile);
+size_t exact_stream_smem(int dtype, int D, int G);
+int exact_stream_warps(int dtype, int D, int G);
+
+// CTAs of the exact streaming kernel: a multiple of Hkv (so a warp keeps one KV
+// head), one per SM up to kExactCtaBound; the workspace is sized for the bound.
+constexpr int kExactCtaBound = 160;
+inline int exact_stream_cta_bound(int hkv) { return hkv > kExactCtaBound ? hkv : (kExactCtaBound / hkv) * hkv; }
+inline int exact_stream_ctas(int hkv, int sms) {
+    const int c = sms >= hkv ? (sms / hkv) * hkv : hkv;
+    const int bound = exact_stream_cta_bound(hkv);
+    return c < bound ? c : bound;
+}
 
 }  // namespace santa
 

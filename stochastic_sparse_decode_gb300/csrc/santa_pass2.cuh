@@ -1,5 +1,5 @@
 // santa_pass2.cuh -- S2ANTA-prop pass 2 (with the global reducer) and the
-// flash / exact merge.
+// S2ANTA-flash merge.
 //
 // prop pass 2 ("Stochastic Sparse Attention for Memory-Bound Inference", paper
 // notes, Key design 2), on the 32-key chunk records of pass 1.  The chunks of
@@ -31,10 +31,9 @@
 // probability anywhere after the softmax.  A tile's budget S_tile (a debug
 // output, with its Z_tile and m_t) is the sum over its chunks.
 //
-// merge (flash, Key design 3; exact split-KV): per (query head, sequence)
-//     flash: out = sum_t w_t o_t / Z   with o_t the tile's sample average,
-//     exact: out = sum_t exp(m_t - M) o_t / Z   with o_t = sum_i e_i V_i,
-// where Z = sum_t w_t.
+// merge (flash, Key design 3): per (query head, sequence)
+//     out = sum_t w_t o_t / Z,   w_t = z_t exp(m_t - M),   Z = sum_t w_t,
+// with o_t the tile's sample average and M the largest tile maximum.
 #pragma once
 
 #include "santa_common.cuh"
@@ -511,7 +510,7 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     }
 }
 
-template <int MODE, int D>
+template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     constexpr int kNW = kMergeThreads / 32;
     const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
@@ -536,10 +535,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
         const int t = c0 + tid;
         float coef = 0.f;
         if (t < Tb) {
-            const float s = expf(__ldcg(p.rec_m + rec0 + t) - M);
-            const float w = __ldcg(p.rec_z + rec0 + t) * s;
-            zpart += w;
-            coef = (MODE == kFlash) ? w : s;
+            coef = __ldcg(p.rec_z + rec0 + t) * expf(__ldcg(p.rec_m + rec0 + t) - M);
+            zpart += coef;
         }
         __syncthreads();
         s_coef[tid] = coef;

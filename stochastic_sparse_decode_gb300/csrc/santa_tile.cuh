@@ -1,4 +1,5 @@
-// santa_tile.cuh -- the split-KV tile kernel shared by the three modes.
+// santa_tile.cuh -- the split-KV tile kernel of S2ANTA-flash, and geometry
+// shared with the streaming kernels.
 //
 // One CTA owns one (sequence b, KV head, tile t) and all G query heads of that
 // KV head's GQA group, so each K row is read once for G heads.  The CTA's four
@@ -17,14 +18,11 @@
 // query head forms the tile's max m_t, the exponentiated scores
 // e_i = exp(x_i - m_t) and their sum z_t -- the tile's partition sum Z_tile on
 // the m_t scale ("Stochastic Sparse Attention for Memory-Bound Inference", paper
-// notes, Key design 2: exponentiated scores plus one Z_tile per tile).  Then:
-//
-//   kFlash  samples S_loc = ceil(S / T_b) systematic thresholds U_t + s/S_loc,
-//           U_t = U S / S_loc, on the tile's own CDF (its prefix of e divided
-//           by z_t), gather-averages the chosen V rows into the tile estimate
-//           and writes it with (m_t, z_t) for the merge (Key design 3).
-//   kExact  streams the tile's V rows through the same slots and accumulates
-//           sum_i e_i V_i for the log-sum-exp merge (exact split-KV decode).
+// notes, Key design 2: exponentiated scores plus one Z_tile per tile).  Then it
+// samples S_loc = ceil(S / T_b) systematic thresholds U_t + s/S_loc,
+// U_t = U S / S_loc, on the tile's own CDF (its prefix of e divided by z_t),
+// gather-averages the chosen V rows into the tile estimate and writes it with
+// (m_t, z_t) for the merge (Key design 3).
 #pragma once
 
 #include "santa_common.cuh"
@@ -54,7 +52,7 @@ __device__ __forceinline__ uint32_t swz(int r, int j) {
 
 // Shared-memory layout of a tile CTA (identical on host and device).  Offsets
 // are from a 1024-byte aligned base; `bytes` includes the alignment slack.
-template <typename T, int D, int G, int MODE>
+template <typename T, int D, int G>
 struct TileSmem {
     static __host__ __device__ int nslot(int tile) { return tile > kRoundKeys ? 2 : 1; }
     static __host__ __device__ size_t q_off(int tile) {
@@ -62,12 +60,10 @@ struct TileSmem {
     }
     static __host__ __device__ size_t xs_off(int tile) { return q_off(tile) + size_t(G) * D * 4; }
     static __host__ __device__ size_t es_off(int tile) { return xs_off(tile) + size_t(G) * tile * 4; }
-    static __host__ __device__ size_t bars_off(int tile) {
-        return es_off(tile) + (MODE == kExact ? size_t(G) * tile * 4 : 0);
-    }
+    static __host__ __device__ size_t bars_off(int tile) { return es_off(tile); }
     static __host__ __device__ size_t red_off(int tile) { return bars_off(tile) + kTileWarps * 2 * 8 + 16; }
     static __host__ __device__ size_t bytes(int tile) {
-        return 1024 + red_off(tile) + (MODE == kExact ? size_t(kTileWarps) * G * D * 4 : 0);
+        return 1024 + red_off(tile);
     }
 };
 
@@ -93,11 +89,10 @@ __device__ __forceinline__ void gather_rows(float (&acc)[D / 32], const T *vrow0
     }
 }
 
-template <int MODE, typename T, int D, int G>
-__global__ void __launch_bounds__(kTileWarps * 32)
-    tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const Params p) {
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kTileWarps * 32) tile_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     using Geo = TileGeom<T, D>;
-    using Lay = TileSmem<T, D, G, MODE>;
+    using Lay = TileSmem<T, D, G>;
     constexpr int kE = D / 32;
     // KV head fastest: the Hkv CTAs of one tile are scheduled together and read
     // the same token rows, so each DRAM page is streamed by them at once.
@@ -139,10 +134,9 @@ __global__ void __launch_bounds__(kTileWarps * 32)
     const int len = min(tile, L - k0);
     const long long tok0 = start + k0;
 
-    // This warp's chunks: rounds r with keys 256 r + 64 warp < len (then, for the
-    // exact mode, the same rounds again for V).
+    // This warp's chunks: rounds r with keys 256 r + 64 warp < len.
     const int nr = len > kWarpRows * warp ? (len - kWarpRows * warp + kRoundKeys - 1) / kRoundKeys : 0;
-    const int nch = (MODE == kExact) ? 2 * nr : nr;
+    const int nch = nr;
     unsigned char *wslots = smem + size_t(warp) * nslot * Geo::kChunkBytes;
     uint64_t *wbars = bars + warp * 2;
 
@@ -155,13 +149,12 @@ __global__ void __launch_bounds__(kTileWarps * 32)
 
     auto issue = [&](int c) {  // lane 0 only
         const int slot = c % nslot;
-        const bool is_v = (MODE == kExact) && c >= nr;
-        const int row = int(tok0) + (is_v ? c - nr : c) * kRoundKeys + warp * kWarpRows;
+        const int row = int(tok0) + c * kRoundKeys + warp * kWarpRows;
         unsigned char *dst = wslots + slot * Geo::kChunkBytes;
         mbar_arrive_expect_tx(&wbars[slot], Geo::kChunkBytes);
 #pragma unroll
         for (int bx = 0; bx < Geo::kBoxes; ++bx)
-            tma_load_3d(dst + bx * kBoxBytes, is_v ? &vmap : &kmap, &wbars[slot], bx * Geo::kBoxElems, kvh, row);
+            tma_load_3d(dst + bx * kBoxBytes, &kmap, &wbars[slot], bx * Geo::kBoxElems, kvh, row);
     };
     int issued = 0;
     if (lane == 0) {
@@ -231,33 +224,21 @@ __global__ void __launch_bounds__(kTileWarps * 32)
     }
     __syncthreads();
 
-    // ---- per-head tile statistics: m_t, e_i = exp(x_i - m_t), z_t (+ the flash sampler)
-    float *es = reinterpret_cast<float *>(smem + Lay::es_off(tile));  // exact: e as [key][G]
+    // ---- per-head tile statistics: m_t, the in-tile prefix of e_i = exp(x_i - m_t), z_t
     for (int h = warp; h < G; h += kTileWarps) {
         float *xh = xs + h * tile;
         float m = -INFINITY;
         for (int i = lane; i < len; i += 32) m = fmaxf(m, xh[i]);
         m = warp_max(m);
-        float z;
         TileScan sc;
-        if constexpr (MODE == kFlash) {
-            for (int i0 = 0; i0 < len; i0 += 32) {
-                const int i = i0 + lane;
-                const float e = (i < len) ? __expf(xh[i] - m) : 0.f;
-                const float P = sc.step(e, i, lane);
-                if (i < len) xh[i] = P;
-            }
-            sc.finish();
-            z = sc.carry;
-        } else {
-            float zl = 0.f;
-            for (int i = lane; i < len; i += 32) {
-                const float e = __expf(xh[i] - m);
-                es[i * G + h] = e;
-                zl += e;
-            }
-            z = warp_sum(zl);
+        for (int i0 = 0; i0 < len; i0 += 32) {
+            const int i = i0 + lane;
+            const float e = (i < len) ? __expf(xh[i] - m) : 0.f;
+            const float P = sc.step(e, i, lane);
+            if (i < len) xh[i] = P;
         }
+        sc.finish();
+        const float z = sc.carry;
         const size_t rec = (size_t(b) * p.Hq + hq0 + h) * p.Tmax + t;
         if (lane == 0) {
             p.rec_m[rec] = m;
@@ -265,7 +246,7 @@ __global__ void __launch_bounds__(kTileWarps * 32)
             if (p.dbg_tile_m) p.dbg_tile_m[rec] = m;
             if (p.dbg_tile_z) p.dbg_tile_z[rec] = z;
         }
-        if constexpr (MODE == kFlash) {
+        {  // the tile's local systematic sample
             __syncwarp();
             const int S_loc = (p.S + Tb - 1) / Tb;
             const float Ut = load_offset(p, b, hq0 + h) * float(p.S) / float(S_loc);
@@ -288,56 +269,6 @@ __global__ void __launch_bounds__(kTileWarps * 32)
 #pragma unroll
             for (int e = 0; e < kE; ++e) p.partial[rec * D + lane * kE + e] = acc[e] * inv;
             if (p.dbg_count && lane == 0) p.dbg_count[rec] = S_loc;
-        }
-    }
-
-    // ---- exact: stream the tile's V rows, o_t = sum_i e_i V_i per head
-    if constexpr (MODE == kExact) {
-        __syncthreads();  // e of every head is in es
-        // this lane's D/32 elements of a row: byte offset lane * kE * kES
-        constexpr int kLaneBytes = kE * Geo::kES;
-        const int jv = (lane * kLaneBytes) >> 4, inner = (lane * kLaneBytes) & 15;
-        float2 acc[G][(kE + 1) / 2];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int q = 0; q < (kE + 1) / 2; ++q) acc[h][q] = make_float2(0.f, 0.f);
-        for (int r = 0; r < nr; ++r) {
-            const int c = nr + r;
-            wait_chunk(c);
-            const unsigned char *base = wslots + (c % nslot) * Geo::kChunkBytes;
-            const int key_base = r * kRoundKeys + warp * kWarpRows;
-            const int nkeys = min(kWarpRows, len - key_base);
-            for (int kk = 0; kk < nkeys; ++kk) {
-                RowSlice<T, D> row;
-                row.load_shared(base + swz(kk, jv) + inner, 0);
-                const float *eh = es + (key_base + kk) * G;
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float e = eh[h];
-                    const float2 ee = make_float2(e, e);
-#pragma unroll
-                    for (int q = 0; q < kE / 2; ++q)
-                        acc[h][q] = __ffma2_rn(ee, make_float2(row.v[2 * q], row.v[2 * q + 1]), acc[h][q]);
-                }
-            }
-            release_chunk(c);
-        }
-        float *red = reinterpret_cast<float *>(smem + Lay::red_off(tile));
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int q = 0; q < kE / 2; ++q) {
-                red[(warp * G + h) * D + lane * kE + 2 * q] = acc[h][q].x;
-                red[(warp * G + h) * D + lane * kE + 2 * q + 1] = acc[h][q].y;
-            }
-        __syncthreads();
-        for (int idx = tid; idx < G * D; idx += kTileWarps * 32) {
-            const int h = idx / D, dd = idx % D;
-            float s = 0.f;
-#pragma unroll
-            for (int w = 0; w < kTileWarps; ++w) s += red[(w * G + h) * D + dd];
-            p.partial[((size_t(b) * p.Hq + hq0 + h) * p.Tmax + t) * D + dd] = s;
         }
     }
 

@@ -60,8 +60,9 @@ def _north_star(sd, **kw):
 
 def test_workspace_layout_matches_the_byte_model(sd):
     """prop: 2 chunk-record arrays [B][Hq][ceil(max_len/32)] and the fp32 score
-    stash [B][Hq][max_len]; flash/exact: 2 tile-record arrays [B][Hq][T] and the
-    tile estimates [B][Hq][T][d]; each rounded up to 256 B."""
+    stash [B][Hq][max_len]; flash: 2 tile-record arrays [B][Hq][T] and the tile
+    estimates [B][Hq][T][d]; exact: the streaming warps' partial states; each
+    rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _north_star(sd)
     T, nch = 32768 // 256, 32768 // 32
@@ -69,7 +70,10 @@ def test_workspace_layout_matches_the_byte_model(sd):
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
     flash = 2 * r(1 * 32 * T * 4) + r(1 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_FLASH) == flash
-    assert sd.workspace_size(p, sd.MODE_EXACT) == flash
+    # exact: (M, Z) and O per (sequence, streaming warp, head of the group); the
+    # streaming grid is at most 160 CTAs of 12 warps for bf16 at d = 128
+    n = 1 * 160 * 12 * 4
+    assert sd.workspace_size(p, sd.MODE_EXACT) == r(n * 8) + r(n * 128 * 4)
     # ragged tail: T = ceil(max_len / tile), chunks = ceil(max_len / 32)
     p = _north_star(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
     T, nch = 8, 32
