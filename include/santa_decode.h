@@ -23,9 +23,11 @@
  *                       systematic samples from its own scores as if it held
  *                       all the mass; a merge rescales the tile estimates by
  *                       Z_tile / Z.  (Same notes, Key design 3.)
- *   exact_decode        exact split-KV decode attention, sum_i A_i V_i, with a
- *                       log-sum-exp merge of the tiles (the dense comparison
- *                       point; same notes, Related work: FlashDecoding).
+ *   exact_decode        exact split-KV decode attention, sum_i A_i V_i: every
+ *                       warp streams a fixed stretch of K and V rows with an
+ *                       online softmax, and a log-sum-exp merge combines the
+ *                       warps a sequence spans (the dense comparison point;
+ *                       same notes, Related work: FlashDecoding).
  *
  * The logit scale is 1/sqrt(d) ("Double-P: Hierarchical Top-P Sparse Attention
  * for Long-Context LLMs", paper review, Stage 1, Eq. 3).  A temperature is
@@ -125,7 +127,7 @@ typedef struct {
     unsigned int *error_flags;   /* device word; kernels OR SANTA_ERR_* bits into it */
     santa_event_t main_begin;    /* recorded on `stream` right before / after the */
     santa_event_t main_end;      /* mode's dominant kernel (prop pass 1, flash tile,
-                                    exact tile), for timing that kernel alone */
+                                    exact stream), for timing that kernel alone */
 } santa_debug;
 
 /*
@@ -187,7 +189,10 @@ int santa_decode_flash(const santa_problem *p, const void *q, const void *k, con
 
 /*
  * Exact split-KV decode: out = sum_i softmax(x)_i V_i, reading all of K and V.
- * Same arguments as santa_decode_prop without U (p->S is ignored).
+ * Same arguments as santa_decode_prop without U (p->S and p->tile are ignored;
+ * of dbg only error_flags, main_begin and main_end are used).  Workspace: per
+ * (sequence slot, warp, query head) a float2 (M, Z) and a D-float partial sum,
+ * for at most 160 rounded to a multiple of num_kv_heads streaming CTAs.
  */
 int exact_decode(const santa_problem *p, const void *q, const void *k, const void *v,
                  const long long *kv_indptr, float *out,

@@ -128,6 +128,57 @@ __device__ __forceinline__ void load_q_slice(const Params &p, int b, int hq0, in
         }
 }
 
+// bf16 keys take their logits from the tensor cores: per chunk, the 32 keys
+// are the A operand (two 16-key tiles, 16 dimensions per fragment, read from the
+// swizzled buffer with ldmatrix) and q is the B operand (16 dimensions x 8
+// heads, heads >= G zero), so a chunk costs 2 D/16 ldmatrix + mma pairs instead
+// of G D / 8 packed FMAs per lane.  Products of bf16 values are exact in fp32;
+// only the order of the fp32 additions differs from a plain dot product.
+//
+// The B fragments of q for heads hq0 .. hq0 + G - 1 of sequence b: lane
+// (g = lane / 4, t = lane % 4) holds dimensions 16 ks + 2t, +1 and 16 ks + 2t + 8,
+// +9 of head hq0 + g.
+template <int D, int G>
+__device__ __forceinline__ void load_q_frag(const Params &p, int b, int hq0, int lane, uint32_t (&qf)[D / 16][2]) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t *qh = reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(p.q) +
+                                                            (size_t(b) * p.Hq + hq0 + min(g, G - 1)) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        qf[ks][0] = g < G ? __ldg(qh + 8 * ks + t) : 0u;
+        qf[ks][1] = g < G ? __ldg(qh + 8 * ks + 4 + t) : 0u;
+    }
+}
+
+// Unscaled logits of the chunk in `base` (32 rows of D bf16 in boxes of 128-byte
+// rows, 128-byte swizzle).  Lane (g, t) ends with c[mt][2 half + j] = q_{2t + j} .
+// k_r for key r = 16 mt + 8 half + g.  The loads are all issued before the
+// first product.
+template <int D>
+__device__ __forceinline__ void chunk_logits_mma(const unsigned char *base, const uint32_t (&qf)[D / 16][2], int lane,
+                                                 float (&c)[2][4]) {
+    constexpr int kKS = D / 16;
+    const int rl = lane & 15, kx = lane >> 4;
+    uint32_t a[2][kKS][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        const int r = mt * 16 + rl;  // lanes 0-7 / 8-15 / 16-23 / 24-31: matrices of rows 0-7, 8-15 at d 0-7, 8-15
+#pragma unroll
+        for (int ks = 0; ks < kKS; ++ks) {
+            const int kv = 2 * ks + kx;  // 16-byte vector of the row: box kv / 8, swizzled slot (kv mod 8) ^ (r mod 8)
+            ldmatrix_x4(a[mt][ks], base + (kv >> 3) * kChunkBoxBytes + r * 128 + (((kv & 7) ^ (r & 7)) << 4));
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[mt][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kKS; ++ks)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) mma_bf16_16816(c[mt], a[mt][ks], qf[ks]);
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     prop_stream_kernel(const __grid_constant__ CUtensorMap kmap, const Params p, int nbuf) {
@@ -135,6 +186,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     using CG = ChunkGeom<T, D, G>;
     constexpr int kGH = CG::kGH, kVPL = CG::kVPL, kKB = CG::kKB, kPairs = Geo::kPairs;
     constexpr int kBG = kGH >= 2 ? 2 : 1;  // batches whose partial sums are reduced together
+    constexpr bool kMma = sizeof(T) == 2;  // bf16 keys: logits on the tensor cores
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g8 = lane >> 3, l8 = lane & 7;
     // the lane's permutation of its reduce-scatter slots (kk, h) -> (kk ^ kx, h ^ hx)
     const int hx = l8 & (kGH - 1), kx = l8 / kGH;
@@ -227,11 +279,15 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
 
     // q of the first chunk is loaded while its keys are in flight
     float2 qreg[kGH][kVPL * kPairs];
+    uint32_t qf[D / 16][2];
     int qb = -1, qkvh = -1;  // whose q the registers hold (one pass only)
-    if (CG::kPasses == 1 && n_issued > 0) {
+    if ((kMma || CG::kPasses == 1) && n_issued > 0) {
         qb = slots[0].b;
         qkvh = slots[0].kvh;
-        load_q_slice<T, D, kGH, kVPL, kPairs>(p, qb, qkvh * G, l8, hx, qreg);
+        if constexpr (kMma)
+            load_q_frag<D, G>(p, qb, qkvh * G, lane, qf);
+        else
+            load_q_slice<T, D, kGH, kVPL, kPairs>(p, qb, qkvh * G, l8, hx, qreg);
     }
 
     bool failed = false;
@@ -251,7 +307,65 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
             continue;
         }
         const unsigned char *base = wbuf + size_t(slot) * CG::kBytes;
-        const long long row0 = cs.start + (long long)ch * kChunkRows;
+        if constexpr (kMma) {
+            if (b != qb || kvh != qkvh) {
+                load_q_frag<D, G>(p, b, kvh * G, lane, qf);
+                qb = b;
+                qkvh = kvh;
+            }
+            float c[2][4];
+            chunk_logits_mma<D>(base, qf, lane, c);
+            // Every lane is done with the buffer: refill it with the next claim.
+            __syncwarp();
+            if (more) claim();
+
+            // Lane (g, t) holds heads 2t + j of keys 8k + g (k = 2 mt + half).  The
+            // chunk's statistics per head are shuffles over the lanes of one t.
+            const int g = lane >> 2, t = lane & 3;
+            float xv[2][4], m[2], z[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    xv[j][k] = 8 * k + g < len ? c[k >> 1][(k & 1) * 2 + j] * p.scale : -INFINITY;
+                m[j] = fmaxf(fmaxf(xv[j][0], xv[j][1]), fmaxf(xv[j][2], xv[j][3]));
+            }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(kFull, m[j], o));
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                z[j] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    xv[j][k] = __expf(xv[j][k] - m[j]);  // 0 for keys past the end
+                    z[j] += xv[j][k];
+                }
+            }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) z[j] += __shfl_xor_sync(kFull, z[j], o);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int h = 2 * t + j;
+                if (h < G) {
+                    const int hq = kvh * G + h;
+                    float *srow = p.stash + (size_t(b) * p.Hq + hq) * p.max_len + size_t(ch) * kChunkRows;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (8 * k + g < len) srow[8 * k + g] = xv[j][k];
+                    if (g == 0) {
+                        const size_t rec = (size_t(b) * p.Hq + hq) * p.nch + ch;
+                        p.rec_m[rec] = m[j];
+                        p.rec_z[rec] = z[j];
+                    }
+                }
+            }
+            ++n_done;
+            continue;
+        }
 #pragma unroll
         for (int hp = 0; hp < CG::kPasses; ++hp) {
             if (CG::kPasses > 1 || b != qb || kvh != qkvh) {
