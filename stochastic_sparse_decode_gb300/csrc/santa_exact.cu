@@ -32,10 +32,10 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
         const size_t s1 = EG::bytes();
         cudaError_t e = ensure_smem(k1, s1);
         if (e != cudaSuccess) return e;
-        if (tm.begin) cudaEventRecord(tm.begin, stream);
+        record_event(tm.begin, stream);
         e = launch_kernel(k1, dim3(unsigned(C)), dim3(EG::kWarps * 32), s1, stream, false, 0, kmap, vmap, p);
         if (e != cudaSuccess) return e;
-        if (tm.end) cudaEventRecord(tm.end, stream);
+        record_event(tm.end, stream);
         return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, false, 0, p, C, int(EG::kWarps));
     });
 }

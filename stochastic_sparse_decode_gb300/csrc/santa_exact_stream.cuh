@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
     constexpr int kBG = kGH >= 2 ? 2 : 1;
     constexpr int kE = D / 32;                          // output elements per lane and head
     constexpr int kLaneBytes = kE * int(sizeof(T));     // 4, 8 or 16
+    constexpr bool kMma = sizeof(T) == 2;               // bf16 keys: logits on the tensor cores
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g8 = lane >> 3, l8 = lane & 7;
     const int hx = l8 & (kGH - 1), kx = l8 / kGH;
     const long long X = (long long)p.B * p.nch * p.Hkv;
@@ -127,8 +128,10 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
 
     // online softmax state of the group's heads for sequence sb
     float Ms[G], Zs[G], O[G][kE];
+    float Mown[2];  // tensor-core layout: M of the lane's own heads 2t, 2t + 1
     int sb = -1;
     auto reset = [&]() {
+        Mown[0] = Mown[1] = -INFINITY;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             Ms[h] = -INFINITY;
@@ -157,6 +160,7 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
         issue(1, cur);
     }
     float2 qreg[kGH][kVPL * kPairs];
+    uint32_t qf[D / 16][2];
     int qb = -1, qkvh = -1;
     uint32_t phK = 0, phV = 0;
     bool failed = false;
@@ -177,7 +181,17 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
         }
         phK ^= 1u;
         float x[CG::kPasses][kGH];
-        if (len > 0) {
+        float c[2][4];  // bf16: the chunk's logits from the tensor cores (layout of chunk_logits_mma)
+        if constexpr (kMma) {
+            if (len > 0) {
+                if (cur.b != qb || cur.kvh != qkvh) {
+                    load_q_frag<D, G>(p, cur.b, cur.kvh * G, lane, qf);
+                    qb = cur.b;
+                    qkvh = cur.kvh;
+                }
+                chunk_logits_mma<D>(kbuf, qf, lane, c);
+            }
+        } else if (len > 0) {
 #pragma unroll
             for (int hp = 0; hp < CG::kPasses; ++hp) {
                 if (CG::kPasses > 1 || cur.b != qb || cur.kvh != qkvh) {
@@ -229,7 +243,53 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
         if (has_next) issue(0, nxt);  // the K buffer is free
 
         // ---- online softmax update; e to the warp's score array
-        if (len > 0) {
+        if constexpr (kMma) {
+          if (len > 0) {
+            // lane (g, t) holds heads 2t + j of keys 8k + g; a head's statistics are
+            // shuffles over the lanes of one t, then broadcast from lane t of group 0
+            const int g = lane >> 2, t = lane & 3;
+            float xv[2][4], m2[2], z2[2], Mn[G], zc[G], mine[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    xv[j][k] = 8 * k + g < len ? c[k >> 1][(k & 1) * 2 + j] * p.scale : -INFINITY;
+                m2[j] = fmaxf(fmaxf(xv[j][0], xv[j][1]), fmaxf(xv[j][2], xv[j][3]));
+            }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) m2[j] = fmaxf(m2[j], __shfl_xor_sync(kFull, m2[j], o));
+#pragma unroll
+            for (int h = 0; h < G; ++h) Mn[h] = fmaxf(Ms[h], __shfl_sync(kFull, m2[h & 1], h >> 1));
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                Mown[j] = fmaxf(Mown[j], m2[j]);  // = Mn[2t + j]
+                mine[j] = Mown[j];
+                z2[j] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float e = __expf(xv[j][k] - mine[j]);  // 0 for keys past the end
+                    if (2 * t + j < G) es[(8 * k + g) * G + 2 * t + j] = e;
+                    z2[j] += e;
+                }
+            }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) z2[j] += __shfl_xor_sync(kFull, z2[j], o);
+#pragma unroll
+            for (int h = 0; h < G; ++h) zc[h] = __shfl_sync(kFull, z2[h & 1], h >> 1);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float sc = __expf(Ms[h] - Mn[h]);  // 0 while the state is empty
+                Zs[h] = fmaf(Zs[h], sc, zc[h]);
+                Ms[h] = Mn[h];
+#pragma unroll
+                for (int e = 0; e < kE; ++e) O[h][e] *= sc;
+            }
+          }
+        } else if (len > 0) {
             float Mn[G], zc[G];
 #pragma unroll
             for (int hp = 0; hp < CG::kPasses; ++hp) {

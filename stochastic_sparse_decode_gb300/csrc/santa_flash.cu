@@ -18,10 +18,10 @@ cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cu
         const size_t s1 = TileSmem<T, D, G>::bytes(p.tile);
         cudaError_t e = ensure_smem(k1, s1);
         if (e != cudaSuccess) return e;
-        if (tm.begin) cudaEventRecord(tm.begin, stream);
+        record_event(tm.begin, stream);
         e = launch_kernel(k1, dim3(p.Hkv, p.Tmax, p.B), dim3(kTileWarps * 32), s1, stream, false, 0, kmap, p);
         if (e != cudaSuccess) return e;
-        if (tm.end) cudaEventRecord(tm.end, stream);
+        record_event(tm.end, stream);
         return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, true, 0, p);
     });
 }

@@ -23,6 +23,17 @@ inline void prop_split(int nch, int tile, int *nsplit, int *cps) {
     *cps = per < unit ? unit : per;
 }
 
+// Records the timing event `ev` (if any) on `stream`.  Inside stream capture it
+// becomes an event-record node of the graph, so a replayed graph is timed too.
+inline void record_event(cudaEvent_t ev, cudaStream_t stream) {
+    if (!ev) return;
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, stream);
+}
+
 // Launches `kern` on `stream`; with `pdl` the kernel may start while the
 // previous kernel in the stream drains (programmatic dependent launch).
 // With cluster_x > 0 the grid's x dimension is cut into thread-block clusters of that size.

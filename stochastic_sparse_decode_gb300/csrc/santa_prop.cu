@@ -74,7 +74,7 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
         const long long chunks = (long long)p.B * p.nch * p.Hkv;
         long long grid = sms >= p.Hkv ? (long long)(sms / p.Hkv) * p.Hkv : sms;
         if (grid > chunks) grid = chunks;
-        if (tm.begin) cudaEventRecord(tm.begin, stream);
+        record_event(tm.begin, stream);
         // Pass 1 may launch early (programmatic dependent launch): behind a previous
         // call's pass 2 it sets up while that kernel drains.  Pass 2 goes in plain
         // stream order -- launched early, its CTAs only wait on SMs pass 1 is using
@@ -82,7 +82,7 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
         // kernel early, 29.4 with both, 30.8 with only pass 2).
         e = launch_kernel(k1, dim3(unsigned(grid)), dim3(kChunkWarps * 32), s1, stream, true, 0, kmap32, p, nbuf);
         if (e != cudaSuccess) return e;
-        if (tm.end) cudaEventRecord(tm.end, stream);
+        record_event(tm.end, stream);
         return launch_kernel(k2, dim3(p.nsplit, p.Hq, p.B), dim3(kPass2Warps * 32), s2, stream, false, p.nsplit, p);
     });
 }
