@@ -153,6 +153,30 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
                       santa_stream_t stream);
 
 /*
+ * The two passes of santa_decode_prop as separate calls (same notes, Key design
+ * 2: pass 1 reads all of K, pass 2 samples from what pass 1 left), for callers
+ * that schedule them apart or time them one by one.  santa_prop_pass1 followed
+ * by santa_prop_pass2 on the same problem, kv_indptr and workspace, in stream
+ * order, gives bit for bit what santa_decode_prop gives.
+ *
+ *   santa_prop_pass1  reads q, K and kv_indptr; writes the chunk records and the
+ *                     score stash into `workspace` (layout of santa_decode_prop);
+ *                     of dbg it uses error_flags, main_begin and main_end.
+ *   santa_prop_pass2  reads the workspace as santa_prop_pass1 left it for the
+ *                     same problem, V, kv_indptr and the offsets U; writes out
+ *                     and dbg's tile and sample outputs.  A workspace that pass 1
+ *                     did not fill for this problem gives undefined values (no
+ *                     fault: every address still comes from the problem).
+ *
+ * Arguments, ownership and errors are those of santa_decode_prop; a pass takes
+ * only the pointers it reads.
+ */
+int santa_prop_pass1(const santa_problem *p, const void *q, const void *k, const long long *kv_indptr,
+                     void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream);
+int santa_prop_pass2(const santa_problem *p, const void *v, const long long *kv_indptr, const float *U, float *out,
+                     void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream);
+
+/*
  * The prop pipeline with the two other samplers of the same notes (Key design 1):
  *
  *   santa_decode_prop_strat   S2ANTA-strat: threshold m is (m + u_m) / S, one

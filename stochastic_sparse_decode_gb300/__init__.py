@@ -26,6 +26,8 @@ ERR_INDPTR, ERR_OFFSET, ERR_TIMEOUT = 1, 2, 4
 EXPORTS = (
     "santa_workspace_size",
     "santa_decode_prop",
+    "santa_prop_pass1",
+    "santa_prop_pass2",
     "santa_decode_prop_strat",
     "santa_decode_prop_iid",
     "santa_decode_flash",
@@ -90,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.santa_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
         for name in ("santa_decode_prop", "santa_decode_prop_strat", "santa_decode_prop_iid", "santa_decode_flash"):
             getattr(L, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
+        L.santa_prop_pass1.argtypes = [P, vp, vp, vp, vp, sz, Dp, vp]
+        L.santa_prop_pass2.argtypes = [P, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.exact_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_decode_prop_static_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, Dp, vp]
         L.santa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint)]
@@ -147,6 +151,16 @@ def santa_decode_prop(problem, q, k, v, kv_indptr, U, out, workspace, debug=None
     """S2ANTA-prop decode: see santa_decode.h.  All tensors on the current CUDA device."""
     _call("santa_decode_prop", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(U), _ptr(out)],
           workspace, debug, stream)
+
+
+def santa_prop_pass1(problem, q, k, kv_indptr, workspace, debug=None, stream=None):
+    """Pass 1 of S2ANTA-prop alone: chunk records and score stash into the workspace."""
+    _call("santa_prop_pass1", problem, [_ptr(q), _ptr(k), _ptr(kv_indptr)], workspace, debug, stream)
+
+
+def santa_prop_pass2(problem, v, kv_indptr, U, out, workspace, debug=None, stream=None):
+    """Pass 2 of S2ANTA-prop alone, on a workspace that santa_prop_pass1 filled."""
+    _call("santa_prop_pass2", problem, [_ptr(v), _ptr(kv_indptr), _ptr(U), _ptr(out)], workspace, debug, stream)
 
 
 def santa_decode_prop_strat(problem, q, k, v, kv_indptr, u, out, workspace, debug=None, stream=None):

@@ -184,17 +184,20 @@ bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long 
 }
 
 // `sampler` (prop only): kSys with offsets U [B][Hq], or kStrat / kIid with uniforms U [B][Hq][S].
+// `stages` (prop only): which of the two passes to run; the other modes run whole.
+// Pass 1 alone needs q, k and kv_indptr; pass 2 alone needs v, kv_indptr, U and out.
 int run(int mode, int sampler, const santa_problem *p, const void *q, const void *k, const void *v,
         const long long *kv_indptr, const float *U, float *out, void *workspace, size_t workspace_bytes,
-        const santa_debug *dbg, santa_stream_t stream_) {
+        const santa_debug *dbg, santa_stream_t stream_, int stages = kPass1 | kPass2) {
     int st = check_problem(p, mode);
     if (st != SANTA_OK) return st;
     if (sampler != kSys && p->S > kMaxSamplerS) return SANTA_UNSUPPORTED;
     if (p->batch == 0) return SANTA_OK;
-    if (!q || !k || !v || !kv_indptr || !out || !workspace) return SANTA_INVALID_ARG;
-    if (mode != SANTA_MODE_EXACT && !U) return SANTA_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(kv_indptr, 8) ||
-        !aligned(workspace, 256) || (U && !aligned(U, 4)))
+    const bool p1 = stages & kPass1, p2 = stages & kPass2;
+    if ((p1 && (!q || !k)) || (p2 && (!v || !out)) || !kv_indptr || !workspace) return SANTA_INVALID_ARG;
+    if (p2 && mode != SANTA_MODE_EXACT && !U) return SANTA_INVALID_ARG;
+    if ((q && !aligned(q, 16)) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) || (out && !aligned(out, 16)) ||
+        !aligned(kv_indptr, 8) || !aligned(workspace, 256) || (U && !aligned(U, 4)))
         return SANTA_INVALID_ARG;
     if (dbg && dbg->sample_stride < 0) return SANTA_INVALID_ARG;
     Layout L;
@@ -207,6 +210,7 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const size_t n_out = size_t(p->batch) * p->num_q_heads * p->head_dim;
     if (L.Tmax == 0 || p->total_tokens == 0) {  // no sequence can hold a key
+        if (!p2) return SANTA_OK;
         const unsigned blocks = unsigned((n_out + 255) / 256 < 1024 ? (n_out + 255) / 256 : 1024);
         zero_out_kernel<<<blocks, 256, 0, stream>>>(out, n_out);
         return cudaGetLastError() == cudaSuccess ? SANTA_OK : SANTA_CUDA_ERROR;
@@ -255,8 +259,9 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
     CUtensorMap kmap, vmap;
     cudaError_t e;
     if (mode == SANTA_MODE_PROP) {
-        if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32)) return SANTA_CUDA_ERROR;
-        e = launch_prop(prm, p->dtype, kmap, stream, tm);
+        if (p1 && !kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32))
+            return SANTA_CUDA_ERROR;
+        e = launch_prop(prm, p->dtype, kmap, stream, tm, stages);
     } else if (mode == SANTA_MODE_FLASH) {
         if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
             return SANTA_CUDA_ERROR;
@@ -291,6 +296,18 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
                       const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
                       santa_stream_t stream) {
     return run(SANTA_MODE_PROP, kSys, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
+}
+
+int santa_prop_pass1(const santa_problem *p, const void *q, const void *k, const long long *kv_indptr,
+                     void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
+    return run(SANTA_MODE_PROP, kSys, p, q, k, nullptr, kv_indptr, nullptr, nullptr, workspace, workspace_bytes, dbg,
+               stream, kPass1);
+}
+
+int santa_prop_pass2(const santa_problem *p, const void *v, const long long *kv_indptr, const float *U, float *out,
+                     void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
+    return run(SANTA_MODE_PROP, kSys, p, nullptr, nullptr, v, kv_indptr, U, out, workspace, workspace_bytes, dbg,
+               stream, kPass2);
 }
 
 int santa_decode_prop_strat(const santa_problem *p, const void *q, const void *k, const void *v,

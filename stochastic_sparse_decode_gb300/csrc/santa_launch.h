@@ -94,7 +94,10 @@ struct Timing {
 
 // Mode launchers (one translation unit each).  `dtype` is SANTA_F32/SANTA_BF16.
 // kmap32: the K descriptor with boxes of 32 rows (the streaming pass-1 kernel).
-cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm);
+// stages: kPass1 | kPass2 (santa_decode_prop runs both, in that order).
+enum { kPass1 = 1, kPass2 = 2 };
+cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm,
+                        int stages);
 cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
 cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          cudaStream_t stream, const Timing &tm);

@@ -53,7 +53,8 @@ static cudaError_t device_limits(int *sms, int *smem_optin) {
     return cudaSuccess;
 }
 
-cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm) {
+cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm,
+                        int stages) {
     int sms = 0, optin = 0;
     cudaError_t e0 = device_limits(&sms, &optin);
     if (e0 != cudaSuccess) return e0;
@@ -74,15 +75,18 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
         const long long chunks = (long long)p.B * p.nch * p.Hkv;
         long long grid = sms >= p.Hkv ? (long long)(sms / p.Hkv) * p.Hkv : sms;
         if (grid > chunks) grid = chunks;
-        record_event(tm.begin, stream);
+        if (stages & kPass1) record_event(tm.begin, stream);
         // Pass 1 may launch early (programmatic dependent launch): behind a previous
         // call's pass 2 it sets up while that kernel drains.  Pass 2 goes in plain
         // stream order -- launched early, its CTAs only wait on SMs pass 1 is using
         // (measured on GB300: 25.3 us per layer-step this way, 26.6 with neither
         // kernel early, 29.4 with both, 30.8 with only pass 2).
-        e = launch_kernel(k1, dim3(unsigned(grid)), dim3(kChunkWarps * 32), s1, stream, true, 0, kmap32, p, nbuf);
-        if (e != cudaSuccess) return e;
-        record_event(tm.end, stream);
+        if (stages & kPass1) {
+            e = launch_kernel(k1, dim3(unsigned(grid)), dim3(kChunkWarps * 32), s1, stream, true, 0, kmap32, p, nbuf);
+            if (e != cudaSuccess) return e;
+            record_event(tm.end, stream);
+        }
+        if (!(stages & kPass2)) return cudaSuccess;
         return launch_kernel(k2, dim3(p.nsplit, p.Hq, p.B), dim3(kPass2Warps * 32), s2, stream, false, p.nsplit, p);
     });
 }

@@ -13,7 +13,7 @@ from __future__ import annotations
 
 import torch
 
-from . import MODES, Debug, decode, make_problem, workspace_size
+from . import MODES, Debug, decode, make_problem, santa_prop_pass1, santa_prop_pass2, workspace_size
 
 
 class Decoder:
@@ -60,4 +60,16 @@ class Decoder:
         if out is None:
             out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=torch.float32, device=self.device)
         decode(mode, p, q, k, v, kv_indptr, U, out, self.workspace(mode), debug, stream)
+        return out
+
+    def pass1(self, q, k, kv_indptr, debug=None, stream=None) -> None:
+        """Pass 1 of prop alone, into the prop workspace (santa_prop_pass1)."""
+        santa_prop_pass1(self.problem, q, k, kv_indptr, self.workspace("prop"), debug, stream)
+
+    def pass2(self, v, kv_indptr, U, out=None, debug=None, stream=None) -> torch.Tensor:
+        """Pass 2 of prop alone, on the prop workspace pass 1 filled (santa_prop_pass2)."""
+        p = self.problem
+        if out is None:
+            out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=torch.float32, device=self.device)
+        santa_prop_pass2(self.problem, v, kv_indptr, U, out, self.workspace("prop"), debug, stream)
         return out

@@ -48,7 +48,38 @@ def test_library_exports_every_declared_symbol(sd):
     lib = sd.lib()
     for n in names:
         assert getattr(lib, n) is not None
+        # every argument typed: an untyped pointer argument would be passed as a 32-bit int
+        assert getattr(lib, n).argtypes is not None, n
     assert set(sd.EXPORTS) == set(names)
+
+
+def test_split_passes_validate_only_what_they_read(sd):
+    p = _north_star(sd)
+    need = sd.workspace_size(p, sd.MODE_PROP)
+    L = sd.lib()
+    dev = 0x10000000  # never dereferenced: every call below is rejected before any launch
+    Q = K = V = U = OUT = IND = dev
+
+    def p1(q=Q, k=K, ind=IND, ws=dev, nbytes=need):
+        return L.santa_prop_pass1(ctypes.byref(p), q, k, ind, ws, nbytes, None, None)
+
+    def p2(v=V, ind=IND, u=U, out=OUT, ws=dev, nbytes=need):
+        return L.santa_prop_pass2(ctypes.byref(p), v, ind, u, out, ws, nbytes, None, None)
+
+    assert p1(q=None) == sd.INVALID_ARG
+    assert p1(k=None) == sd.INVALID_ARG
+    assert p1(ind=None) == sd.INVALID_ARG
+    assert p1(k=dev + 8) == sd.INVALID_ARG
+    assert p1(nbytes=need - 1) == sd.WORKSPACE_TOO_SMALL
+    assert p2(v=None) == sd.INVALID_ARG
+    assert p2(u=None) == sd.INVALID_ARG
+    assert p2(out=None) == sd.INVALID_ARG
+    assert p2(ws=dev + 128) == sd.INVALID_ARG
+    assert p2(nbytes=need - 1) == sd.WORKSPACE_TOO_SMALL
+    # batch 0 is a no-op for either pass
+    p0 = _north_star(sd, batch=0)
+    assert L.santa_prop_pass1(ctypes.byref(p0), None, None, None, None, 0, None, None) == sd.OK
+    assert L.santa_prop_pass2(ctypes.byref(p0), None, None, None, None, None, 0, None, None) == sd.OK
 
 
 def _north_star(sd, **kw):

@@ -1,0 +1,62 @@
+"""The two passes of S2ANTA-prop called one by one through the C ABI.
+
+"Stochastic Sparse Attention for Memory-Bound Inference" (paper notes, Key
+design 2) splits prop into pass 1 (read all of K; stash the exponentiated
+scores and the partition records) and pass 2 (reduce, sample, gather V).
+santa_prop_pass1 followed by santa_prop_pass2 must give bit for bit what
+santa_decode_prop gives, on a ragged batch (empty, one-key and tail-chunk
+sequences) and on the 32k Llama-3.1-8B layer; and pass 2 alone must read
+only what pass 1 left, so re-running pass 2 gives the same result again.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from synthetic import Workload, generate, get_workload, to_torch
+
+from santa_harness import decoder_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from stochastic_sparse_decode_gb300.build import build
+
+    build()
+
+
+def _both_ways(inp):
+    dec = decoder_for(inp)
+    q, k, v, indptr, U = to_torch(inp)
+    dbg1, b1 = dec.debug_buffers("prop")
+    whole = dec("prop", q, k, v, indptr, U, debug=dbg1).clone()
+    torch.cuda.synchronize()
+    dbg2, b2 = dec.debug_buffers("prop")
+    dec.workspace("prop").fill_(0xA5)  # nothing of the whole call may carry over
+    dec.pass1(q, k, indptr, debug=dbg2)
+    split = dec.pass2(v, indptr, U, debug=dbg2).clone()
+    again = dec.pass2(v, indptr, U).clone()
+    torch.cuda.synchronize()
+    assert int(b1["error_flags"][0]) == 0 and int(b2["error_flags"][0]) == 0
+    return whole, split, again, b1, b2
+
+
+@pytest.mark.parametrize("name", ["ragged_edges", "llama8b_32k_b1"])
+def test_pass1_then_pass2_matches_whole_call(name):
+    if name == "ragged_edges":
+        w = Workload(name="passes_ragged", config=41, batch=5, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                     tile=64, S=50, dtype="bf16", lengths=(0, 1, 33, 300, 2500))
+    else:
+        w = get_workload(name)
+    inp = generate(w)
+    whole, split, again, b1, b2 = _both_ways(inp)
+    assert torch.equal(whole, split)
+    assert torch.equal(whole, again)
+    for key in ("sample_idx", "tile_count"):
+        assert torch.equal(b1[key], b2[key]), key
+    for key in ("tile_m", "tile_z"):
+        assert torch.equal(torch.nan_to_num(b1[key], nan=-7.0), torch.nan_to_num(b2[key], nan=-7.0)), key
