@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -153,6 +154,25 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&a)[4], const void *row) {
                  : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
                  : "r"(smem_addr(row))
                  : "memory");
+}
+
+// The same with each 8x8 matrix transposed on the way: lane (g, t) receives the
+// elements (rows 2t, 2t + 1; column g) of matrix j in register j.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&a)[4], const void *row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                 : "r"(smem_addr(row))
+                 : "memory");
+}
+
+// Two floats as a bf16 pair (x in the low half), each rounded to nearest even,
+// and the pair of what the rounding left out, also as bf16 (x = hi + lo to
+// about 2^-16 relative).
+__device__ __forceinline__ void bf16_split2(float x, float y, uint32_t *hi, uint32_t *lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
+    *hi = *reinterpret_cast<const uint32_t *>(&h);
+    *lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 // d += A B on the tensor cores: A 16x16 bf16 (row-major fragment), B 16x8 bf16
@@ -321,10 +341,10 @@ __device__ __forceinline__ void raise_flag(const Params &p, unsigned bit) {
     if (p.err) atomicOr(p.err, bit);
 }
 
-// Start and length of sequence b; an inconsistent kv_indptr entry gives an
-// empty sequence and raises SANTA_ERR_INDPTR.
-__device__ __forceinline__ int seq_bounds(const Params &p, int b, long long *start) {
-    const long long s = p.kv_indptr[b], e = p.kv_indptr[b + 1];
+// Start and length of a sequence from its kv_indptr entries s = kv_indptr[b],
+// e = kv_indptr[b + 1]; an inconsistent pair gives an empty sequence and raises
+// SANTA_ERR_INDPTR.
+__device__ __forceinline__ int checked_bounds(const Params &p, long long s, long long e, long long *start) {
     if (s < 0 || e < s || e > p.total_tokens || e - s > (long long)p.max_len) {
         raise_flag(p, SANTA_ERR_INDPTR);
         *start = 0;
@@ -333,16 +353,21 @@ __device__ __forceinline__ int seq_bounds(const Params &p, int b, long long *sta
     *start = s;
     return int(e - s);
 }
+__device__ __forceinline__ int seq_bounds(const Params &p, int b, long long *start) {
+    return checked_bounds(p, p.kv_indptr[b], p.kv_indptr[b + 1], start);
+}
 
-// Offset U of (b, h), clamped into [0, 1/S) (SANTA_ERR_OFFSET if it was not).
-__device__ __forceinline__ float load_offset(const Params &p, int b, int h) {
-    float u = p.U[b * p.Hq + h];
+// An offset U clamped into [0, 1/S) (SANTA_ERR_OFFSET if it was not).
+__device__ __forceinline__ float checked_offset(const Params &p, float u) {
     if (!(u >= 0.f) || double(u) * double(p.S) >= 1.0) {
         raise_flag(p, SANTA_ERR_OFFSET);
         u = (u >= 0.f) ? nextafterf(1.0f / float(p.S), 0.f) : 0.f;
         while (double(u) * double(p.S) >= 1.0) u = nextafterf(u, 0.f);
     }
     return u;
+}
+__device__ __forceinline__ float load_offset(const Params &p, int b, int h) {
+    return checked_offset(p, p.U[b * p.Hq + h]);
 }
 
 }  // namespace santa

@@ -128,10 +128,14 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
 
     // online softmax state of the group's heads for sequence sb
     float Ms[G], Zs[G], O[G][kE];
-    float Mown[2];  // tensor-core layout: M of the lane's own heads 2t, 2t + 1
+    // bf16, tensor-core layout: lane (g, t) owns heads 2t, 2t + 1 (Mown: their M)
+    // and holds O^T in m16n8 tiles: Ot[m] = O[2t, 2t + 1][16 m + g] and [.. + 8]
+    float Mown[2], Ot[kMma ? D / 16 : 1][4];
     int sb = -1;
     auto reset = [&]() {
         Mown[0] = Mown[1] = -INFINITY;
+#pragma unroll
+        for (int m = 0; m < (kMma ? D / 16 : 1); ++m) Ot[m][0] = Ot[m][1] = Ot[m][2] = Ot[m][3] = 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             Ms[h] = -INFINITY;
@@ -143,11 +147,26 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
     auto flush = [&]() {  // this warp's partial of sequence sb (its KV head is c mod Hkv)
         if (sb < 0) return;
         const size_t slot = (size_t(sb) * P + W) * G;
+        if constexpr (kMma) {
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (2 * t + j < G) {
+                    float *o = p.partial + (slot + 2 * t + j) * D + g;
+#pragma unroll
+                    for (int m = 0; m < D / 16; ++m) {
+                        o[16 * m] = Ot[m][j];
+                        o[16 * m + 8] = Ot[m][2 + j];
+                    }
+                }
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float *o = p.partial + (slot + h) * D + lane * kE;
+            if constexpr (!kMma) {
+                float *o = p.partial + (slot + h) * D + lane * kE;
 #pragma unroll
-            for (int e = 0; e < kE; ++e) o[e] = O[h][e];
+                for (int e = 0; e < kE; ++e) o[e] = O[h][e];
+            }
             if (lane == 0) reinterpret_cast<float2 *>(p.rec_m)[slot + h] = make_float2(Ms[h], Zs[h]);
         }
     };
@@ -262,9 +281,12 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
                 for (int j = 0; j < 2; ++j) m2[j] = fmaxf(m2[j], __shfl_xor_sync(kFull, m2[j], o));
 #pragma unroll
             for (int h = 0; h < G; ++h) Mn[h] = fmaxf(Ms[h], __shfl_sync(kFull, m2[h & 1], h >> 1));
+            float sco[2];  // rescale of the lane's own heads
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
+                const float mold = Mown[j];
                 Mown[j] = fmaxf(Mown[j], m2[j]);  // = Mn[2t + j]
+                sco[j] = __expf(mold - Mown[j]);  // 0 while the state is empty
                 mine[j] = Mown[j];
                 z2[j] = 0.f;
 #pragma unroll
@@ -285,8 +307,13 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
                 const float sc = __expf(Ms[h] - Mn[h]);  // 0 while the state is empty
                 Zs[h] = fmaf(Zs[h], sc, zc[h]);
                 Ms[h] = Mn[h];
+            }
 #pragma unroll
-                for (int e = 0; e < kE; ++e) O[h][e] *= sc;
+            for (int m = 0; m < D / 16; ++m) {
+                Ot[m][0] *= sco[0];
+                Ot[m][1] *= sco[1];
+                Ot[m][2] *= sco[0];
+                Ot[m][3] *= sco[1];
             }
           }
         } else if (len > 0) {
@@ -334,7 +361,38 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
             break;
         }
         phV ^= 1u;
-        if (len > 0) {
+        if constexpr (kMma) {
+            // O^T += V^T P^T on the tensor cores: A = V^T (16 dims x 16 keys, read
+            // transposed from the swizzled V buffer), B = P^T (16 keys x 8 heads,
+            // heads >= G zero) from the score array, split into bf16 high and low
+            // parts so that e keeps ~16 bits.  Keys past the chunk's end have e = 0.
+            if (len > 0) {
+                const int g = lane >> 2, t = lane & 3, mq = lane >> 3, mi = lane & 7;
+                uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int key = 16 * ks + 8 * hf + 2 * t;
+                        const float e0 = g < G ? es[key * G + g] : 0.f;
+                        const float e1 = g < G ? es[(key + 1) * G + g] : 0.f;
+                        bf16_split2(e0, e1, &bh[ks][hf], &bl[ks][hf]);
+                    }
+#pragma unroll
+                for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        // matrix mq: keys 16 ks + 8 (mq / 2) + row, dims 16 m + 8 (mq % 2) ..
+                        const int key = 16 * ks + 8 * (mq >> 1) + mi;
+                        const int dv = 2 * m + (mq & 1);  // 16-byte vector of the row
+                        uint32_t a[4];
+                        ldmatrix_x4_trans(a, vbuf + (dv >> 3) * kChunkBoxBytes + key * 128 +
+                                                 (((dv & 7) ^ (key & 7)) << 4));
+                        mma_bf16_16816(Ot[m], a, bh[ks]);
+                        mma_bf16_16816(Ot[m], a, bl[ks]);
+                    }
+            }
+        } else if (len > 0) {
             // this lane's D/32 elements of a row: box, 16-byte vector and offset in it
             const int lb0 = lane * kLaneBytes;
             const unsigned char *vlane = vbuf + (lb0 >> 7) * kChunkBoxBytes + (lb0 & 15);

@@ -239,10 +239,13 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
         ev[k] = (k < kper && key < p.max_len) ? __ldcg(sseq + key) : 0.f;
     }
     // Inputs the previous kernel does not write may be read before the dependency wait
-    // (pass 1 lets this kernel start only once its own predecessor is complete).
+    // (pass 1 lets this kernel start only once its own predecessor is complete).  All
+    // loads are issued before any of them is checked: one round trip, not two.
+    const long long ind0 = p.kv_indptr[b], ind1 = p.kv_indptr[b + 1];
+    const float u_raw = SAMPLER == kSys ? p.U[size_t(b) * p.Hq + hq] : 0.f;
     long long start;
-    const int L = seq_bounds(p, b, &start);
-    const float u = SAMPLER == kSys ? load_offset(p, b, hq) : 0.f;
+    const int L = checked_bounds(p, ind0, ind1, &start);
+    const float u = SAMPLER == kSys ? checked_offset(p, u_raw) : 0.f;
     if constexpr (SAMPLER != kSys) {
         // the head's S uniforms, each checked into [0, 1); the i.i.d. ones sorted
         int nu = 1;
