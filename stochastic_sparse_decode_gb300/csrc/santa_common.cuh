@@ -20,6 +20,7 @@ constexpr int kWarpRows = 64;    // K/V rows per TMA chunk of one tile-kernel wa
 constexpr int kPass2Warps = 8;   // warps of a prop pass-2 CTA
 constexpr int kMaxSplit = 8;     // prop pass 2: CTAs per head = size of its cluster
 constexpr int kMergeThreads = 128;
+constexpr int kExactCtaBound = 160;  // exact: streaming CTAs at most (the workspace is sized for it)
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
 
 enum Mode { kProp = 0, kFlash = 1, kExact = 2 };

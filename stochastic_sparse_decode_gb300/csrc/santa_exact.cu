@@ -36,7 +36,7 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
         e = launch_kernel(k1, dim3(unsigned(C)), dim3(EG::kWarps * 32), s1, stream, false, 0, kmap, vmap, p);
         if (e != cudaSuccess) return e;
         record_event(tm.end, stream);
-        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, false, 0, p, C, int(EG::kWarps));
+        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kExactMergeWarps * 32), 0, stream, false, 0, p, C, int(EG::kWarps));
     });
 }
 

@@ -476,14 +476,22 @@ __global__ void __launch_bounds__(ExactStreamGeom<T, D, G>::kWarps * 32, 1)
 // Log-sum-exp merge of one (query head, sequence): the partials (M_w, Z_w, O_w) of
 // the warps whose walk touched the sequence (W = w C + c with c = kvh mod Hkv),
 // in a fixed order: out = sum_w exp(M_w - M) O_w / sum_w exp(M_w - M) Z_w.
+// One CTA of 16 warps per head: the coefficients of all candidates first (one
+// round trip for the (M, Z) pairs), then warp k sums candidates k, k + 16, ...
+// with all its partial rows in flight at once, then the warps in order.
+constexpr int kExactMergeWarps = 16;
+constexpr int kExactMergeMax = kExactCtaBound * 12;  // candidates: warps per CTA x CTAs of one KV head
+
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) exact_stream_merge(const Params p, int C, int warps) {
-    constexpr int kNW = kMergeThreads / 32;
-    const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+__global__ void __launch_bounds__(kExactMergeWarps * 32) exact_stream_merge(const Params p, int C, int warps) {
+    constexpr int kE = D / 32;
+    constexpr int kT = kExactMergeWarps * 32;
+    const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kvh = hq / p.G, h = hq % p.G;
-    __shared__ float s_coef[kMergeThreads];
-    __shared__ int s_w[kMergeThreads];
-    __shared__ float scr[kNW];
+    __shared__ float s_coef[kExactMergeMax];
+    __shared__ int s_w[kExactMergeMax];
+    __shared__ float red[kExactMergeWarps][D];
+    __shared__ float scr[kExactMergeWarps];
 
     long long start;
     const int L = seq_bounds(p, b, &start);
@@ -494,44 +502,75 @@ __global__ void __launch_bounds__(kMergeThreads) exact_stream_merge(const Params
     }
     const long long P = (long long)C * warps;
     const long long X = (long long)p.B * p.nch * p.Hkv, per_seq = (long long)p.nch * p.Hkv;
-    const int per_w = C / p.Hkv;                // CTAs of this KV head
-    const int ncand = warps * per_w;
-    auto cand = [&](int i) -> long long { return (long long)(i / per_w) * C + kvh + (long long)(i % per_w) * p.Hkv; };
+    const int per_w = C / p.Hkv;  // CTAs of this KV head
+    const int ncand = min(warps * per_w, kExactMergeMax);
     const float2 *mz = reinterpret_cast<const float2 *>(p.rec_m);
     const size_t base = size_t(b) * P;
 
+    // (M_w, Z_w) of every candidate; M, then the coefficients exp(M_w - M)
+    float mw[kExactMergeMax / kT + 1], zw[kExactMergeMax / kT + 1];
     float mx = -INFINITY;
-    for (int i = tid; i < ncand; i += kMergeThreads) {
-        const long long Wi = cand(i);
-        if (exact_touches(Wi, P, X, per_seq, b)) mx = fmaxf(mx, __ldcg(&mz[(base + Wi) * p.G + h].x));
-    }
-    const float M = block_max<kNW>(mx, scr);
-    float num = 0.f, zpart = 0.f;
-    for (int c0 = 0; c0 < ncand; c0 += kMergeThreads) {
-        const int i = c0 + tid;
-        float coef = 0.f;
-        int wi = 0;
+#pragma unroll
+    for (int k = 0; k * kT < kExactMergeMax; ++k) {
+        const int i = tid + k * kT;
+        mw[k] = -INFINITY;
+        zw[k] = 0.f;
         if (i < ncand) {
-            const long long Wi = cand(i);
-            wi = int(Wi);
+            const long long Wi = (long long)(i / per_w) * C + kvh + (long long)(i % per_w) * p.Hkv;
+            s_w[i] = int(Wi);
             if (exact_touches(Wi, P, X, per_seq, b)) {
                 const float2 v = __ldcg(&mz[(base + Wi) * p.G + h]);
-                coef = v.x > -INFINITY ? expf(v.x - M) : 0.f;
-                zpart = fmaf(v.y, coef, zpart);
+                mw[k] = v.x;
+                zw[k] = v.y;
             }
         }
-        __syncthreads();
-        s_coef[tid] = coef;
-        s_w[tid] = wi;
-        __syncthreads();
-        const int n = min(kMergeThreads, ncand - c0);
-        if (tid < D)
-            for (int k = 0; k < n; ++k)
-                if (s_coef[k] != 0.f)
-                    num = fmaf(s_coef[k], __ldcg(p.partial + ((base + s_w[k]) * p.G + h) * D + tid), num);
+        mx = fmaxf(mx, mw[k]);
     }
-    const float Z = block_sum<kNW>(zpart, scr);
-    if (tid < D) outp[tid] = num / Z;
+    const float M = block_max<kExactMergeWarps>(mx, scr);
+    float zpart = 0.f;
+#pragma unroll
+    for (int k = 0; k * kT < kExactMergeMax; ++k) {
+        const int i = tid + k * kT;
+        if (i < ncand) {
+            const float cf = mw[k] > -INFINITY ? expf(mw[k] - M) : 0.f;
+            s_coef[i] = cf;
+            zpart = fmaf(zw[k], cf, zpart);
+        }
+    }
+    const float Z = block_sum<kExactMergeWarps>(zpart, scr);  // its barriers also publish s_coef / s_w
+
+    float acc[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) acc[e] = 0.f;
+    for (int i0 = warp; i0 < ncand; i0 += 8 * kExactMergeWarps) {
+        float v[8][kE], cf[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kExactMergeWarps;
+            cf[u] = i < ncand ? s_coef[i] : 0.f;
+            if (cf[u] != 0.f) {
+                const float *src = p.partial + ((base + s_w[i]) * p.G + h) * D + lane * kE;
+#pragma unroll
+                for (int e = 0; e < kE; ++e) v[u][e] = __ldcg(src + e);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kE; ++e) v[u][e] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int e = 0; e < kE; ++e) acc[e] = fmaf(cf[u], v[u][e], acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < kE; ++e) red[warp][lane * kE + e] = acc[e];
+    __syncthreads();
+    if (tid < D) {
+        float num = 0.f;
+#pragma unroll
+        for (int w = 0; w < kExactMergeWarps; ++w) num += red[w][tid];
+        outp[tid] = num / Z;
+    }
 }
 
 }  // namespace santa

@@ -111,7 +111,6 @@ int exact_stream_warps(int dtype, int D, int G);
 
 // CTAs of the exact streaming kernel: a multiple of Hkv (so a warp keeps one KV
 // head), one per SM up to kExactCtaBound; the workspace is sized for the bound.
-constexpr int kExactCtaBound = 160;
 inline int exact_stream_cta_bound(int hkv) { return hkv > kExactCtaBound ? hkv : (kExactCtaBound / hkv) * hkv; }
 inline int exact_stream_ctas(int hkv, int sms) {
     const int c = sms >= hkv ? (sms / hkv) * hkv : hkv;
