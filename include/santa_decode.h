@@ -177,6 +177,39 @@ int santa_prop_pass2(const santa_problem *p, const void *v, const long long *kv_
                      void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream);
 
 /*
+ * A paged K / V cache (page-table indirection, as serving systems keep it).
+ * The pools hold num_pages pages of page_size keys: K and V are
+ * [num_pages * page_size][num_kv_heads][head_dim] in the problem's dtype, that
+ * is the contiguous layout with total_tokens = num_pages * page_size rows.  Key
+ * i of sequence b is row page_table[b * max_pages + i / page_size] * page_size
+ * + i % page_size; sequence b holds kv_lens[b] keys.
+ */
+typedef struct {
+    const int *page_table;   /* device [B][max_pages] int32 page ids */
+    const int *kv_lens;      /* device [B] int32 sequence lengths, each <= max_len */
+    int page_size;           /* keys per page, a positive multiple of 32 */
+    int max_pages;           /* row length of page_table; max_len <= max_pages * page_size */
+    long long num_pages;     /* pages in each pool; num_pages * page_size == total_tokens */
+} santa_pages;
+
+/*
+ * S2ANTA-prop decode (same notes, Key designs 1-2) on a paged cache; the pages
+ * themselves only claim compatibility with paged serving (Overall framework).
+ * Same arguments as santa_decode_prop with k_pool / v_pool for k / v and the
+ * page table for kv_indptr; workspace: santa_workspace_size with
+ * SANTA_MODE_PROP.  A page size that is not a multiple of 32, a pool size that
+ * disagrees with total_tokens or a max_len beyond a page-table row is
+ * SANTA_INVALID_ARG.  On the device, a length outside [0, max_len] makes the
+ * sequence empty and a page id outside [0, num_pages) drops that page's keys
+ * (pass 1) or reads row 0 (pass 2); both raise SANTA_ERR_INDPTR.  A chunk of 32
+ * keys never straddles two pages, so the results equal those of
+ * santa_decode_prop on the same keys laid out contiguously, bit for bit.
+ */
+int santa_decode_prop_paged(const santa_problem *p, const santa_pages *pages, const void *q, const void *k_pool,
+                            const void *v_pool, const float *U, float *out, void *workspace, size_t workspace_bytes,
+                            const santa_debug *dbg, santa_stream_t stream);
+
+/*
  * The prop pipeline with the two other samplers of the same notes (Key design 1):
  *
  *   santa_decode_prop_strat   S2ANTA-strat: threshold m is (m + u_m) / S, one

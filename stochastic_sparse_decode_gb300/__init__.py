@@ -28,6 +28,7 @@ EXPORTS = (
     "santa_decode_prop",
     "santa_prop_pass1",
     "santa_prop_pass2",
+    "santa_decode_prop_paged",
     "santa_decode_prop_strat",
     "santa_decode_prop_iid",
     "santa_decode_flash",
@@ -75,6 +76,18 @@ class Debug(ctypes.Structure):
     ]
 
 
+class Pages(ctypes.Structure):
+    """santa_pages"""
+
+    _fields_ = [
+        ("page_table", ctypes.c_void_p),
+        ("kv_lens", ctypes.c_void_p),
+        ("page_size", ctypes.c_int),
+        ("max_pages", ctypes.c_int),
+        ("num_pages", ctypes.c_longlong),
+    ]
+
+
 _lib = None
 
 
@@ -94,6 +107,7 @@ def lib() -> ctypes.CDLL:
             getattr(L, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_prop_pass1.argtypes = [P, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_prop_pass2.argtypes = [P, vp, vp, vp, vp, vp, sz, Dp, vp]
+        L.santa_decode_prop_paged.argtypes = [P, ctypes.POINTER(Pages), vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.exact_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_decode_prop_static_scratch.argtypes = [P, vp, vp, vp, vp, vp, vp, Dp, vp]
         L.santa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint)]
@@ -161,6 +175,22 @@ def santa_prop_pass1(problem, q, k, kv_indptr, workspace, debug=None, stream=Non
 def santa_prop_pass2(problem, v, kv_indptr, U, out, workspace, debug=None, stream=None):
     """Pass 2 of S2ANTA-prop alone, on a workspace that santa_prop_pass1 filled."""
     _call("santa_prop_pass2", problem, [_ptr(v), _ptr(kv_indptr), _ptr(U), _ptr(out)], workspace, debug, stream)
+
+
+def make_pages(page_table, kv_lens, page_size, num_pages) -> Pages:
+    """santa_pages for device tensors page_table [B][max_pages] and kv_lens [B] (int32)."""
+    return Pages(int(page_table.data_ptr()), int(kv_lens.data_ptr()), int(page_size), int(page_table.shape[-1]),
+                 int(num_pages))
+
+
+def santa_decode_prop_paged(problem, pages, q, k_pool, v_pool, U, out, workspace, debug=None, stream=None):
+    """S2ANTA-prop decode on a paged cache: see santa_decode.h."""
+    dbg = ctypes.byref(debug) if debug is not None else None
+    st = lib().santa_decode_prop_paged(ctypes.byref(problem), ctypes.byref(pages), _ptr(q), _ptr(k_pool),
+                                       _ptr(v_pool), _ptr(U), _ptr(out), _ptr(workspace), _nbytes(workspace), dbg,
+                                       _stream(stream))
+    if st != OK:
+        raise SantaError(st, "santa_decode_prop_paged")
 
 
 def santa_decode_prop_strat(problem, q, k, v, kv_indptr, u, out, workspace, debug=None, stream=None):

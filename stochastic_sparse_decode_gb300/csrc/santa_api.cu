@@ -186,18 +186,31 @@ bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long 
 // `sampler` (prop only): kSys with offsets U [B][Hq], or kStrat / kIid with uniforms U [B][Hq][S].
 // `stages` (prop only): which of the two passes to run; the other modes run whole.
 // Pass 1 alone needs q, k and kv_indptr; pass 2 alone needs v, kv_indptr, U and out.
+// `pages` (prop only): a paged cache; k and v are then the page pools and kv_indptr is unused.
 int run(int mode, int sampler, const santa_problem *p, const void *q, const void *k, const void *v,
         const long long *kv_indptr, const float *U, float *out, void *workspace, size_t workspace_bytes,
-        const santa_debug *dbg, santa_stream_t stream_, int stages = kPass1 | kPass2) {
+        const santa_debug *dbg, santa_stream_t stream_, int stages = kPass1 | kPass2,
+        const santa_pages *pages = nullptr) {
     int st = check_problem(p, mode);
     if (st != SANTA_OK) return st;
     if (sampler != kSys && p->S > kMaxSamplerS) return SANTA_UNSUPPORTED;
+    if (pages) {
+        if (mode != SANTA_MODE_PROP || pages->page_size <= 0 || pages->page_size % 32 != 0 || pages->max_pages <= 0 ||
+            pages->num_pages <= 0 || pages->num_pages > kMaxTokens / pages->page_size ||
+            pages->num_pages * pages->page_size != p->total_tokens ||
+            (long long)p->max_len > (long long)pages->max_pages * pages->page_size)
+            return SANTA_INVALID_ARG;
+    }
     if (p->batch == 0) return SANTA_OK;
     const bool p1 = stages & kPass1, p2 = stages & kPass2;
-    if ((p1 && (!q || !k)) || (p2 && (!v || !out)) || !kv_indptr || !workspace) return SANTA_INVALID_ARG;
+    if (pages && (!pages->page_table || !pages->kv_lens || !aligned(pages->page_table, 4) ||
+                  !aligned(pages->kv_lens, 4)))
+        return SANTA_INVALID_ARG;
+    if ((p1 && (!q || !k)) || (p2 && (!v || !out)) || (!kv_indptr && !pages) || !workspace)
+        return SANTA_INVALID_ARG;
     if (p2 && mode != SANTA_MODE_EXACT && !U) return SANTA_INVALID_ARG;
     if ((q && !aligned(q, 16)) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) || (out && !aligned(out, 16)) ||
-        !aligned(kv_indptr, 8) || !aligned(workspace, 256) || (U && !aligned(U, 4)))
+        (kv_indptr && !aligned(kv_indptr, 8)) || !aligned(workspace, 256) || (U && !aligned(U, 4)))
         return SANTA_INVALID_ARG;
     if (dbg && dbg->sample_stride < 0) return SANTA_INVALID_ARG;
     Layout L;
@@ -233,7 +246,14 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
     prm.q = q;
     prm.k = k;
     prm.v = v;
-    prm.kv_indptr = kv_indptr;
+    prm.kv_indptr = pages ? nullptr : kv_indptr;
+    if (pages) {
+        prm.page_table = pages->page_table;
+        prm.kv_lens = pages->kv_lens;
+        prm.page_size = pages->page_size;
+        prm.max_pages = pages->max_pages;
+        prm.num_pages = pages->num_pages;
+    }
     prm.U = sampler == kSys ? U : nullptr;
     prm.u_samples = sampler == kSys ? nullptr : U;
     prm.sampler = sampler;
@@ -308,6 +328,14 @@ int santa_prop_pass2(const santa_problem *p, const void *v, const long long *kv_
                      void *workspace, size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
     return run(SANTA_MODE_PROP, kSys, p, nullptr, nullptr, v, kv_indptr, U, out, workspace, workspace_bytes, dbg,
                stream, kPass2);
+}
+
+int santa_decode_prop_paged(const santa_problem *p, const santa_pages *pages, const void *q, const void *k_pool,
+                            const void *v_pool, const float *U, float *out, void *workspace, size_t workspace_bytes,
+                            const santa_debug *dbg, santa_stream_t stream) {
+    if (!pages) return SANTA_INVALID_ARG;
+    return run(SANTA_MODE_PROP, kSys, p, q, k_pool, v_pool, nullptr, U, out, workspace, workspace_bytes, dbg, stream,
+               kPass1 | kPass2, pages);
 }
 
 int santa_decode_prop_strat(const santa_problem *p, const void *q, const void *k, const void *v,

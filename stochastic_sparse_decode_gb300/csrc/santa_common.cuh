@@ -38,6 +38,13 @@ struct Params {
     float scale;  // 1/sqrt(d)
     const void *q, *k, *v;
     const long long *kv_indptr;
+    // paged KV cache (prop): key i of sequence b is row
+    // page_table[b * max_pages + i / page_size] * page_size + i % page_size of the
+    // K / V pools, and its length is kv_lens[b]; null page_table: contiguous
+    // cache addressed by kv_indptr
+    const int *page_table, *kv_lens;
+    int page_size, max_pages;
+    long long num_pages;
     const float *U;          // prop (systematic) / flash: offsets [B][Hq] in [0, 1/S)
     const float *u_samples;  // prop stratified / i.i.d.: uniforms [B][Hq][S] in [0, 1)
     float *out;
@@ -354,8 +361,35 @@ __device__ __forceinline__ int checked_bounds(const Params &p, long long s, long
     *start = s;
     return int(e - s);
 }
+// The raw bounds of sequence b: (kv_indptr[b], kv_indptr[b + 1]), or (0, kv_lens[b])
+// for a paged cache (whose length must also fit its page-table row).
+__device__ __forceinline__ void raw_bounds(const Params &p, int b, long long *s, long long *e) {
+    if (p.page_table) {
+        const long long L = p.kv_lens[b];
+        *s = 0;
+        *e = L <= (long long)p.max_pages * p.page_size ? L : -1;  // -1: rejected below
+    } else {
+        *s = p.kv_indptr[b];
+        *e = p.kv_indptr[b + 1];
+    }
+}
 __device__ __forceinline__ int seq_bounds(const Params &p, int b, long long *start) {
-    return checked_bounds(p, p.kv_indptr[b], p.kv_indptr[b + 1], start);
+    long long s, e;
+    raw_bounds(p, b, &s, &e);
+    return checked_bounds(p, s, e, start);
+}
+
+// Row of the K / V cache that holds key i of sequence b (start: the sequence's
+// first row, contiguous layout).  A page id outside [0, num_pages) raises
+// SANTA_ERR_INDPTR and gives -1.
+__device__ __forceinline__ long long key_row(const Params &p, int b, long long start, int i) {
+    if (!p.page_table) return start + i;
+    const int pg = __ldg(p.page_table + (size_t)b * p.max_pages + i / p.page_size);
+    if (pg < 0 || pg >= p.num_pages) {
+        raise_flag(p, SANTA_ERR_INDPTR);
+        return -1;
+    }
+    return (long long)pg * p.page_size + i % p.page_size;
 }
 
 // An offset U clamped into [0, 1/S) (SANTA_ERR_OFFSET if it was not).

@@ -256,7 +256,19 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 lL = seq_bounds(p, b, &lstart);
                 lb = b;
             }
-            const int len = min(kChunkRows, lL - ch * kChunkRows);
+            int len = min(kChunkRows, lL - ch * kChunkRows);
+            long long row = 0;
+            if (len > 0) {
+                row = key_row(p, b, lstart, ch * kChunkRows);  // a chunk never straddles pages
+                if (row < 0) {  // bad page id (flagged): the chunk carries no mass
+                    for (int h = 0; h < G; ++h) {
+                        const size_t rec = (size_t(b) * p.Hq + kvh * G + h) * p.nch + ch;
+                        p.rec_m[rec] = -INFINITY;
+                        p.rec_z[rec] = 0.f;
+                    }
+                    len = 0;
+                }
+            }
             const int slot = n_issued % nbuf;
             slots[slot] = ChunkSlot{lstart, b, ch, kvh, len};
             uint64_t *bar = &bars[slot];
@@ -266,8 +278,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 mbar_arrive_expect_tx(bar, CG::kBytes);
 #pragma unroll
                 for (int bx = 0; bx < Geo::kBoxes; ++bx)
-                    tma_load_3d(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, kvh,
-                                int(lstart) + ch * kChunkRows);
+                    tma_load_3d(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, kvh, int(row));
             } else {
                 mbar_arrive(bar);
             }

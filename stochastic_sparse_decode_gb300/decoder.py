@@ -13,7 +13,8 @@ from __future__ import annotations
 
 import torch
 
-from . import MODES, Debug, decode, make_problem, santa_prop_pass1, santa_prop_pass2, workspace_size
+from . import (MODES, Debug, decode, make_pages, make_problem, santa_decode_prop_paged, santa_prop_pass1,
+               santa_prop_pass2, workspace_size)
 
 
 class Decoder:
@@ -72,4 +73,15 @@ class Decoder:
         if out is None:
             out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=torch.float32, device=self.device)
         santa_prop_pass2(self.problem, v, kv_indptr, U, out, self.workspace("prop"), debug, stream)
+        return out
+
+    def prop_paged(self, q, k_pool, v_pool, page_table, kv_lens, page_size, U, out=None, debug=None,
+                   stream=None) -> torch.Tensor:
+        """S2ANTA-prop on a paged cache (santa_decode_prop_paged); the problem's
+        total_tokens must be the pools' rows, num_pages * page_size."""
+        p = self.problem
+        if out is None:
+            out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=torch.float32, device=self.device)
+        pages = make_pages(page_table, kv_lens, page_size, p.total_tokens // page_size)
+        santa_decode_prop_paged(p, pages, q, k_pool, v_pool, U, out, self.workspace("prop"), debug, stream)
         return out

@@ -230,3 +230,25 @@ def test_missing_library_fails_loudly(monkeypatch, sd):
     monkeypatch.setattr(sd, "LIB_PATH", "/nonexistent/libsanta_decode.so")
     with pytest.raises(RuntimeError, match="missing"):
         sd.lib()
+
+
+def test_paged_problems_are_validated_before_any_launch(sd):
+    L = sd.lib()
+    dev = 0x10000000  # never dereferenced: every call below is rejected before any launch
+    p = _north_star(sd, total_tokens=512 * 64)
+    need = sd.workspace_size(p, sd.MODE_PROP)
+
+    def call(page_size=64, max_pages=512, num_pages=512, table=dev, lens=dev, prob=p, nbytes=need):
+        pg = sd.Pages(table, lens, page_size, max_pages, num_pages)
+        return L.santa_decode_prop_paged(ctypes.byref(prob), ctypes.byref(pg), dev, dev, dev, dev, dev, dev, nbytes,
+                                         None, None)
+
+    assert call(page_size=48) == sd.INVALID_ARG                    # not a multiple of 32
+    assert call(page_size=0) == sd.INVALID_ARG
+    assert call(num_pages=511) == sd.INVALID_ARG                   # pools disagree with total_tokens
+    assert call(max_pages=511) == sd.INVALID_ARG                   # max_len beyond a page-table row
+    assert call(table=None) == sd.INVALID_ARG
+    assert call(lens=dev + 2) == sd.INVALID_ARG                    # kv_lens not 4-byte aligned
+    assert call(nbytes=need - 1) == sd.WORKSPACE_TOO_SMALL
+    assert L.santa_decode_prop_paged(ctypes.byref(p), None, dev, dev, dev, dev, dev, dev, need, None,
+                                     None) == sd.INVALID_ARG
