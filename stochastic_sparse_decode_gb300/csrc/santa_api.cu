@@ -103,7 +103,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     return SANTA_OK;
 }
 
-int smem_check(const santa_problem *p, int mode, int sampler) {
+int smem_check(const santa_problem *p, int mode, int sampler, bool paged) {
     constexpr size_t kOptin = 227 * 1024;  // shared memory a block may opt in to on sm_103
     const int G = p->num_q_heads / p->num_kv_heads;
     size_t need = 0;
@@ -111,7 +111,7 @@ int smem_check(const santa_problem *p, int mode, int sampler) {
         Layout L;
         if (make_layout(p, mode, &L) != SANTA_OK) return SANTA_INVALID_ARG;
         need = prop_pass1_smem(p->dtype, p->head_dim, G, int(kOptin));
-        const size_t s2 = prop_pass2_smem(p->head_dim, L.cps, sampler, p->S);
+        const size_t s2 = prop_pass2_smem(p->head_dim, L.cps, sampler, p->S, paged);
         if (s2 > need) need = s2;
     } else if (mode == SANTA_MODE_FLASH) {
         need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
@@ -217,7 +217,7 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
     st = make_layout(p, mode, &L);
     if (st != SANTA_OK) return st;
     if (workspace_bytes < L.total) return SANTA_WORKSPACE_TOO_SMALL;
-    st = smem_check(p, mode, sampler);
+    st = smem_check(p, mode, sampler, pages != nullptr);
     if (st != SANTA_OK) return st;
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

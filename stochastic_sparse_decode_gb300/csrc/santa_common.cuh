@@ -38,13 +38,6 @@ struct Params {
     float scale;  // 1/sqrt(d)
     const void *q, *k, *v;
     const long long *kv_indptr;
-    // paged KV cache (prop): key i of sequence b is row
-    // page_table[b * max_pages + i / page_size] * page_size + i % page_size of the
-    // K / V pools, and its length is kv_lens[b]; null page_table: contiguous
-    // cache addressed by kv_indptr
-    const int *page_table, *kv_lens;
-    int page_size, max_pages;
-    long long num_pages;
     const float *U;          // prop (systematic) / flash: offsets [B][Hq] in [0, 1/S)
     const float *u_samples;  // prop stratified / i.i.d.: uniforms [B][Hq][S] in [0, 1)
     float *out;
@@ -62,6 +55,13 @@ struct Params {
     int *dbg_count, *dbg_idx;
     int dbg_stride;
     unsigned int *err;
+    // paged KV cache (prop): key i of sequence b is row
+    // page_table[b * max_pages + i / page_size] * page_size + i % page_size of the
+    // K / V pools, and its length is kv_lens[b]; null page_table: contiguous
+    // cache addressed by kv_indptr
+    const int *page_table, *kv_lens;
+    int page_size, max_pages;
+    long long num_pages;
 };
 
 // ------------------------------------------------------------------ PTX
@@ -363,8 +363,9 @@ __device__ __forceinline__ int checked_bounds(const Params &p, long long s, long
 }
 // The raw bounds of sequence b: (kv_indptr[b], kv_indptr[b + 1]), or (0, kv_lens[b])
 // for a paged cache (whose length must also fit its page-table row).
+template <bool kPaged = false>
 __device__ __forceinline__ void raw_bounds(const Params &p, int b, long long *s, long long *e) {
-    if (p.page_table) {
+    if constexpr (kPaged) {
         const long long L = p.kv_lens[b];
         *s = 0;
         *e = L <= (long long)p.max_pages * p.page_size ? L : -1;  // -1: rejected below
@@ -373,17 +374,19 @@ __device__ __forceinline__ void raw_bounds(const Params &p, int b, long long *s,
         *e = p.kv_indptr[b + 1];
     }
 }
+template <bool kPaged = false>
 __device__ __forceinline__ int seq_bounds(const Params &p, int b, long long *start) {
     long long s, e;
-    raw_bounds(p, b, &s, &e);
+    raw_bounds<kPaged>(p, b, &s, &e);
     return checked_bounds(p, s, e, start);
 }
 
 // Row of the K / V cache that holds key i of sequence b (start: the sequence's
 // first row, contiguous layout).  A page id outside [0, num_pages) raises
 // SANTA_ERR_INDPTR and gives -1.
+template <bool kPaged>
 __device__ __forceinline__ long long key_row(const Params &p, int b, long long start, int i) {
-    if (!p.page_table) return start + i;
+    if constexpr (!kPaged) return start + i;
     const int pg = __ldg(p.page_table + (size_t)b * p.max_pages + i / p.page_size);
     if (pg < 0 || pg >= p.num_pages) {
         raise_flag(p, SANTA_ERR_INDPTR);

@@ -104,7 +104,7 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
 
 // Shared-memory needs, for validation on the host.
 size_t prop_pass1_smem(int dtype, int D, int G, int smem_optin);
-size_t prop_pass2_smem(int D, int cps, int sampler, int S);
+size_t prop_pass2_smem(int D, int cps, int sampler, int S, bool paged);
 size_t flash_tile_smem(int dtype, int D, int G, int tile);
 size_t exact_stream_smem(int dtype, int D, int G);
 int exact_stream_warps(int dtype, int D, int G);

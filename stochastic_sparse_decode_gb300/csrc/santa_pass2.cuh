@@ -132,11 +132,13 @@ struct Pass2Smem {
     static __host__ __device__ size_t wl_off(int cps) { return last_off(cps) + size_t(kPass2Warps) * kP2Batch * 4; }
     static __host__ __device__ size_t red_off(int cps) { return wl_off(cps) + size_t(kPass2Warps) * 32 * 4; }
     static __host__ __device__ size_t part_off(int cps) { return red_off(cps) + size_t(kPass2Warps) * D * 4; }
-    static __host__ __device__ size_t pg_off(int cps) { return part_off(cps) + size_t(kMaxSplit) * D * 4; }
-    // page ids of a CTA's keys (paged cache; page_size >= 32, so at most cps + 1 of them)
-    static __host__ __device__ size_t u_off(int cps) { return pg_off(cps) + size_t(cps + 2) * 4; }
+    static __host__ __device__ size_t u_off(int cps) { return part_off(cps) + size_t(kMaxSplit) * D * 4; }
     // nu: the head's uniforms (stratified / i.i.d. samplers), padded to a power of two; 0 otherwise
-    static __host__ __device__ size_t bytes(int cps, int nu) { return u_off(cps) + size_t(nu) * 4; }
+    static __host__ __device__ size_t pg_off(int cps, int nu) { return u_off(cps) + size_t(nu) * 4; }
+    // paged cache: the page ids of a CTA's keys (page_size >= 32, so at most cps + 1 of them)
+    static __host__ __device__ size_t bytes(int cps, int nu, bool paged = false) {
+        return pg_off(cps, nu) + (paged ? size_t(cps + 2) * 4 : 0);
+    }
 };
 
 constexpr int kRankSortMax = 512;  // i.i.d. uniforms up to this many are sorted by rank
@@ -187,7 +189,7 @@ __device__ __forceinline__ void block_bitonic_sort(float *a, int n) {
         }
 }
 
-template <typename T, int D, int SAMPLER>
+template <typename T, int D, int SAMPLER, bool kPaged>
 __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const Params p) {
     constexpr int kThreads = kPass2Warps * 32;
     constexpr int kE = D / 32;
@@ -211,7 +213,8 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     float *red = reinterpret_cast<float *>(smem + Lay::red_off(cps));
     float *part = reinterpret_cast<float *>(smem + Lay::part_off(cps));
     float *s_u = reinterpret_cast<float *>(smem + Lay::u_off(cps));  // stratified / i.i.d. uniforms
-    int *s_pg = reinterpret_cast<int *>(smem + Lay::pg_off(cps));    // paged cache: this CTA's page ids
+    // paged cache: this CTA's page ids (systematic sampler only: no uniforms before them)
+    int *s_pg = reinterpret_cast<int *>(smem + Lay::pg_off(cps, 0));
 
     pdl_launch_dependents();  // the next call's pass 1 may start its prologue on free SMs
     cluster_arrive();         // first half of the barrier that makes every CTA's shared memory addressable
@@ -245,13 +248,16 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
     // (pass 1 lets this kernel start only once its own predecessor is complete).  All
     // loads are issued before any of them is checked: one round trip, not two.
     long long ind0, ind1;
-    raw_bounds(p, b, &ind0, &ind1);
+    raw_bounds<kPaged>(p, b, &ind0, &ind1);
     const float u_raw = SAMPLER == kSys ? p.U[size_t(b) * p.Hq + hq] : 0.f;
     // paged cache: the page ids of this CTA's keys, kept in shared memory
-    const int ps = max(p.page_size, 1), key_lo = split * cps * kChunkRows;
-    const int pg_lo = key_lo / ps;
-    const int npg = p.page_table ? min(p.max_pages, (key_lo + cps * kChunkRows - 1) / ps + 1) - pg_lo : 0;
-    for (int i = tid; i < npg; i += kThreads) s_pg[i] = __ldg(p.page_table + size_t(b) * p.max_pages + pg_lo + i);
+    int pg_lo = 0;
+    if constexpr (kPaged) {
+        const int key_lo = split * cps * kChunkRows;
+        pg_lo = key_lo / p.page_size;
+        const int npg = min(p.max_pages, (key_lo + cps * kChunkRows - 1) / p.page_size + 1) - pg_lo;
+        for (int i = tid; i < npg; i += kThreads) s_pg[i] = __ldg(p.page_table + size_t(b) * p.max_pages + pg_lo + i);
+    }
     long long start;
     const int L = checked_bounds(p, ind0, ind1, &start);
     const float u = SAMPLER == kSys ? checked_offset(p, u_raw) : 0.f;
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
                     const int len = min(kChunkRows, L - c * kChunkRows);
                     const int j = c * kChunkRows + cdf_search(wev + k * 32, len, r, wlast[k]);
                     int row = j;  // row of V relative to vseq
-                    if (p.page_table) {
+                    if constexpr (kPaged) {
                         const int pg = s_pg[j / p.page_size - pg_lo];
                         if (pg < 0 || pg >= p.num_pages) {  // bad page id: flagged, row 0 read instead
                             raise_flag(p, SANTA_ERR_INDPTR);

@@ -18,17 +18,18 @@ size_t prop_pass1_smem(int dtype, int d, int g, int smem_optin) {
     return bytes;
 }
 
-size_t prop_pass2_smem(int d, int cps, int sampler, int S) {
+size_t prop_pass2_smem(int d, int cps, int sampler, int S, bool paged) {
     const int nu = sampler_slots(sampler, S);
-    return d == 128 ? Pass2Smem<uint16_t, 128>::bytes(cps, nu) : Pass2Smem<uint16_t, 64>::bytes(cps, nu);
+    return d == 128 ? Pass2Smem<uint16_t, 128>::bytes(cps, nu, paged) : Pass2Smem<uint16_t, 64>::bytes(cps, nu, paged);
 }
 
 template <typename T, int D>
-static void *pass2_for(int sampler) {
+static void *pass2_for(int sampler, bool paged) {
+    if (paged) return sampler == kSys ? reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys, true>) : nullptr;
     switch (sampler) {
-        case kSys: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys>);
-        case kStrat: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kStrat>);
-        case kIid: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kIid>);
+        case kSys: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys, false>);
+        case kStrat: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kStrat, false>);
+        case kIid: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kIid, false>);
         default: return nullptr;
     }
 }
@@ -62,11 +63,11 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
         using CG = ChunkGeom<T, D, G>;
         const int nbuf = CG::nbuf_for(size_t(optin));
         if (!nbuf) return cudaErrorNotSupported;
-        auto k1 = prop_stream_kernel<T, D, G>;
+        auto k1 = p.page_table ? prop_stream_kernel<T, D, G, true> : prop_stream_kernel<T, D, G, false>;
         const size_t s1 = CG::bytes(nbuf);
-        auto k2 = reinterpret_cast<void (*)(const Params)>(pass2_for<T, D>(p.sampler));
+        auto k2 = reinterpret_cast<void (*)(const Params)>(pass2_for<T, D>(p.sampler, p.page_table != nullptr));
         if (!k2) return cudaErrorInvalidValue;
-        const size_t s2 = Pass2Smem<T, D>::bytes(p.chunks_per_split, sampler_slots(p.sampler, p.S));
+        const size_t s2 = Pass2Smem<T, D>::bytes(p.chunks_per_split, sampler_slots(p.sampler, p.S), p.page_table);
         cudaError_t e = ensure_smem(k1, s1);
         if (e == cudaSuccess) e = ensure_smem(k2, s2);
         if (e != cudaSuccess) return e;

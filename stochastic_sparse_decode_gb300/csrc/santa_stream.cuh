@@ -179,7 +179,7 @@ __device__ __forceinline__ void chunk_logits_mma(const unsigned char *base, cons
         for (int mt = 0; mt < 2; ++mt) mma_bf16_16816(c[mt], a[mt][ks], qf[ks]);
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kPaged>
 __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     prop_stream_kernel(const __grid_constant__ CUtensorMap kmap, const Params p, int nbuf) {
     using Geo = TileGeom<T, D>;
@@ -253,13 +253,13 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 ch = int(r - (long long)b * p.nch);
             }
             if (b != lb) {
-                lL = seq_bounds(p, b, &lstart);
+                lL = seq_bounds<kPaged>(p, b, &lstart);
                 lb = b;
             }
             int len = min(kChunkRows, lL - ch * kChunkRows);
-            long long row = 0;
-            if (len > 0) {
-                row = key_row(p, b, lstart, ch * kChunkRows);  // a chunk never straddles pages
+            long long row = lstart + ch * kChunkRows;
+            if (kPaged && len > 0) {
+                row = key_row<kPaged>(p, b, lstart, ch * kChunkRows);  // a chunk never straddles pages
                 if (row < 0) {  // bad page id (flagged): the chunk carries no mass
                     for (int h = 0; h < G; ++h) {
                         const size_t rec = (size_t(b) * p.Hq + kvh * G + h) * p.nch + ch;
