@@ -164,9 +164,10 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
  *                     of dbg it uses error_flags, main_begin and main_end.
  *   santa_prop_pass2  reads the workspace as santa_prop_pass1 left it for the
  *                     same problem, V, kv_indptr and the offsets U; writes out
- *                     and dbg's tile and sample outputs.  A workspace that pass 1
- *                     did not fill for this problem gives undefined values (no
- *                     fault: every address still comes from the problem).
+ *                     and dbg's tile and sample outputs.  It must follow
+ *                     santa_prop_pass1 on the same problem and workspace in
+ *                     stream order: on a workspace that pass 1 did not fill, the
+ *                     chunk records are arbitrary and the behaviour is undefined.
  *
  * Arguments, ownership and errors are those of santa_decode_prop; a pass takes
  * only the pointers it reads.
