@@ -54,7 +54,7 @@ def test_library_exports_every_declared_symbol(sd):
 
 
 def test_split_passes_validate_only_what_they_read(sd):
-    p = _north_star(sd)
+    p = _llama8b_problem(sd)
     need = sd.workspace_size(p, sd.MODE_PROP)
     L = sd.lib()
     dev = 0x10000000  # never dereferenced: every call below is rejected before any launch
@@ -77,12 +77,12 @@ def test_split_passes_validate_only_what_they_read(sd):
     assert p2(ws=dev + 128) == sd.INVALID_ARG
     assert p2(nbytes=need - 1) == sd.WORKSPACE_TOO_SMALL
     # batch 0 is a no-op for either pass
-    p0 = _north_star(sd, batch=0)
+    p0 = _llama8b_problem(sd, batch=0)
     assert L.santa_prop_pass1(ctypes.byref(p0), None, None, None, None, 0, None, None) == sd.OK
     assert L.santa_prop_pass2(ctypes.byref(p0), None, None, None, None, None, 0, None, None) == sd.OK
 
 
-def _north_star(sd, **kw):
+def _llama8b_problem(sd, **kw):
     args = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, total_tokens=32768, max_len=32768,
                 tile=256, S=128, dtype="bf16")
     args.update(kw)
@@ -95,7 +95,7 @@ def test_workspace_layout_matches_the_byte_model(sd):
     estimates [B][Hq][T][d]; exact: the streaming warps' partial states; each
     rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    p = _north_star(sd)
+    p = _llama8b_problem(sd)
     T, nch = 32768 // 256, 32768 // 32
     prop = 2 * r(1 * 32 * nch * 4) + r(32 * 32768 * 4)
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
@@ -106,7 +106,7 @@ def test_workspace_layout_matches_the_byte_model(sd):
     n = 1 * 160 * 12 * 4
     assert sd.workspace_size(p, sd.MODE_EXACT) == r(n * 8) + r(n * 128 * 4)
     # ragged tail: T = ceil(max_len / tile), chunks = ceil(max_len / 32)
-    p = _north_star(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
+    p = _llama8b_problem(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
     T, nch = 8, 32
     assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_PROP) == 2 * r(3 * 32 * nch * 4) + r(3 * 32 * 1000 * 4)
@@ -115,7 +115,7 @@ def test_workspace_layout_matches_the_byte_model(sd):
 def test_very_long_prop_contexts_are_unsupported_not_wrong(sd):
     """Pass 2 keeps a CTA's share of the chunk records in shared memory: a max_len
     past that is refused on the host (flash and exact still take it)."""
-    p = _north_star(sd, max_len=32 * 1024 * 1024, total_tokens=32 * 1024 * 1024, tile=1024)
+    p = _llama8b_problem(sd, max_len=32 * 1024 * 1024, total_tokens=32 * 1024 * 1024, tile=1024)
     n = ctypes.c_size_t(0)
     assert sd.lib().santa_workspace_size(ctypes.byref(p), sd.MODE_PROP, ctypes.byref(n)) == sd.OK
     assert _call_prop(sd, p) == sd.UNSUPPORTED
@@ -136,7 +136,7 @@ def test_very_long_prop_contexts_are_unsupported_not_wrong(sd):
     ("total_tokens", 1 << 40, "INVALID_ARG"),
 ])
 def test_bad_problems_are_rejected(sd, field, value, status):
-    p = _north_star(sd)
+    p = _llama8b_problem(sd)
     setattr(p, field, value)
     n = ctypes.c_size_t(0)
     st = sd.lib().santa_workspace_size(ctypes.byref(p), sd.MODE_PROP, ctypes.byref(n))
@@ -144,7 +144,7 @@ def test_bad_problems_are_rejected(sd, field, value, status):
 
 
 def test_exact_ignores_S(sd):
-    p = _north_star(sd, S=0)
+    p = _llama8b_problem(sd, S=0)
     assert sd.workspace_size(p, sd.MODE_EXACT) > 0
     with pytest.raises(sd.SantaError):
         sd.workspace_size(p, sd.MODE_PROP)
@@ -179,7 +179,7 @@ def _call_prop(sd, p, q=0x10000, k=0x20000, v=0x30000, ind=0x40000, U=0x50000, o
 
 
 def test_null_misaligned_and_small_workspace_are_rejected(sd):
-    p = _north_star(sd)
+    p = _llama8b_problem(sd)
     assert _call_prop(sd, p, q=None) == sd.INVALID_ARG
     assert _call_prop(sd, p, U=None) == sd.INVALID_ARG
     assert _call_prop(sd, p, out=None) == sd.INVALID_ARG
@@ -189,7 +189,7 @@ def test_null_misaligned_and_small_workspace_are_rejected(sd):
     need = sd.workspace_size(p, sd.MODE_PROP)
     assert _call_prop(sd, p, ws_bytes=need - 1) == sd.WORKSPACE_TOO_SMALL
     # batch 0 is a no-op that touches nothing
-    assert _call_prop(sd, _north_star(sd, batch=0), q=None, k=None) == sd.OK
+    assert _call_prop(sd, _llama8b_problem(sd, batch=0), q=None, k=None) == sd.OK
 
 
 @pytest.mark.parametrize("name", ["santa_decode_prop_strat", "santa_decode_prop_iid"])
@@ -197,13 +197,13 @@ def test_sampler_modes_refuse_more_uniforms_than_shared_memory_holds(sd, name):
     """The stratified and i.i.d. samplers keep a head's S uniforms on chip: S <= 16384."""
     t = _FakeTensor
     for S, status in ((16385, sd.UNSUPPORTED), (1 << 20, sd.UNSUPPORTED)):
-        p = _north_star(sd, S=S)
+        p = _llama8b_problem(sd, S=S)
         ws = sd.workspace_size(p, sd.MODE_PROP)
         with pytest.raises(sd.SantaError) as e:
             getattr(sd, name)(p, t(0x10000), t(0x20000), t(0x30000), t(0x40000), t(0x50000), t(0x60000),
                               t(0x100000, ws), stream=0)
         assert e.value.status == status
-    p = _north_star(sd, S=64)
+    p = _llama8b_problem(sd, S=64)
     with pytest.raises(sd.SantaError) as e:  # null uniforms
         getattr(sd, name)(p, t(0x10000), t(0x20000), t(0x30000), t(0x40000), None, t(0x60000),
                           t(0x100000, sd.workspace_size(p, sd.MODE_PROP)), stream=0)
@@ -211,7 +211,7 @@ def test_sampler_modes_refuse_more_uniforms_than_shared_memory_holds(sd, name):
 
 
 def test_exact_needs_no_offsets(sd):
-    p = _north_star(sd)
+    p = _llama8b_problem(sd)
     ws = sd.workspace_size(p, sd.MODE_EXACT)
     with pytest.raises(sd.SantaError) as e:
         sd.exact_decode(p, _FakeTensor(0x10000), _FakeTensor(0x20000), _FakeTensor(0x30000), None,
@@ -235,7 +235,7 @@ def test_missing_library_fails_loudly(monkeypatch, sd):
 def test_paged_problems_are_validated_before_any_launch(sd):
     L = sd.lib()
     dev = 0x10000000  # never dereferenced: every call below is rejected before any launch
-    p = _north_star(sd, total_tokens=512 * 64)
+    p = _llama8b_problem(sd, total_tokens=512 * 64)
     need = sd.workspace_size(p, sd.MODE_PROP)
 
     def call(page_size=64, max_pages=512, num_pages=512, table=dev, lens=dev, prob=p, nbytes=need):

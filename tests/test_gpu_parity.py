@@ -107,15 +107,15 @@ def test_one_hot_returns_the_row_exactly():
 
 
 @pytest.fixture(scope="module")
-def north_star():
+def llama8b_layer():
     inp = generate(get_workload("llama8b_32k_b1"))
     return inp, to_torch(inp)
 
 
 @pytest.mark.parametrize("mode,S", [("prop", 128), ("prop", 256), ("flash", 2048), ("flash", 128), ("exact", 0)])
-def test_llama8b_32k_batch1(north_star, mode, S):
+def test_llama8b_32k_batch1(llama8b_layer, mode, S):
     """batch 1, 32 q / 8 KV heads, d=128, n_k=32768, tile 256: every head against the oracle."""
-    inp, dev = north_star
+    inp, dev = llama8b_layer
     if S and S != inp.workload.S:
         U = draw_offsets(S, (1, 1, 32), np.random.default_rng(S))[0]
         res = run(inp, mode, S=S, dev_inputs=dev[:4] + (torch.from_numpy(U).cuda(),))
@@ -126,9 +126,9 @@ def test_llama8b_32k_batch1(north_star, mode, S):
     _report(f"llama8b_32k_b1/{mode}/S{S}", rep)
 
 
-def test_prop_is_deterministic(north_star):
+def test_prop_is_deterministic(llama8b_layer):
     """Two calls give bit-identical outputs (fixed-order combine, no float atomics)."""
-    inp, dev = north_star
+    inp, dev = llama8b_layer
     a = run(inp, "prop", dev_inputs=dev, debug=False)["out"]
     b = run(inp, "prop", dev_inputs=dev, debug=False)["out"]
     assert np.array_equal(a, b)

@@ -356,7 +356,7 @@ def test_monte_carlo_convergence_and_variance_ordering():
 # ------------------------------------------------------------- page figures
 
 
-def test_page_figures_and_north_star_v_row_fraction():
+def test_page_figures_and_llama8b_v_row_fraction():
     """The byte model and sample fractions the pages state, and the V-row bound
     (at most 4 S distinct rows per KV head, < 1.56% at 32k) on the synthetic
     Llama-3.1-8B layer."""
