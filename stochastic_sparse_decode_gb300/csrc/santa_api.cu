@@ -55,6 +55,17 @@ int check_problem(const santa_problem *p, int mode) {
 //   exact:       per (sequence, streaming warp, head of the group) the partial state
 //                (M, Z) as rec_m [B][P][G][2] and O as [B][P][G][d], P the warps of
 //                the streaming kernel's largest grid.
+// SMs of the current device (152 on GB300, also the answer without a device).
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();  // leave no sticky error behind on a machine without a device
+        return 152;
+    }
+    return n;
+}
+
 int make_layout(const santa_problem *p, int mode, Layout *L) {
     const int Tmax = (p->max_len + p->tile - 1) / p->tile;
     const int nch = (p->max_len + 31) / 32;
@@ -87,7 +98,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     size_t off = 0;
     L->Tmax = Tmax;
     L->nch = nch;
-    prop_split(nch, p->tile, &L->nsplit, &L->cps);
+    prop_split(nch, p->tile, (long long)p->batch * p->num_q_heads, sm_count(), &L->nsplit, &L->cps);
     L->rec_m = off;
     off += align256(n_rec * 4);
     L->rec_z = off;

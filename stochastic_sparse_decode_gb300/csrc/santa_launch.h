@@ -12,10 +12,17 @@ namespace santa {
 
 // prop pass 2: CTAs per head (a cluster of at most kMaxSplit) and 32-key chunks
 // per CTA -- whole tiles (so a tile's debug totals stay in one CTA) and a
-// multiple of the warp count; about 128 chunks (16 per warp) per CTA.
-inline void prop_split(int nch, int tile, int *nsplit, int *cps) {
+// multiple of the warp count.  About 128 chunks (16 per warp) per CTA while the
+// heads are too few to fill the GPU; with `heads` (batch x query heads) enough for
+// two CTAs per SM on their own, fewer splits, because every split re-runs the
+// head's reducer.  At most 8192 chunks per CTA (their records sit in shared memory).
+inline void prop_split(int nch, int tile, long long heads, int sms, int *nsplit, int *cps) {
     const int unit = (tile / 32) > kPass2Warps ? tile / 32 : kPass2Warps;
     int n = (nch + 127) / 128;
+    const long long fill = heads > 0 ? (2LL * sms + heads - 1) / heads : 1;  // splits for two CTAs per SM
+    if (n > fill) n = int(fill);
+    const int n_smem = (nch + 8191) / 8192;
+    if (n < n_smem) n = n_smem;
     n = n < 1 ? 1 : (n > kMaxSplit ? kMaxSplit : n);
     int per = (nch + n - 1) / n;
     per = (per + unit - 1) / unit * unit;
