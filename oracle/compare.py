@@ -2,9 +2,10 @@
 
 Numpy only.  Acceptance rules (same U on both sides):
 
-* sampled indices and tile budgets bit-exact, except where a threshold lies
-  within 1e-5 (relative) of a CDF boundary separating the two answers, measured
-  in the oracle's float64 CDF -- such mismatches are excused and counted;
+* sampled indices and tile budgets bit-exact, except where the threshold lies
+  within 1e-5 (relative) of EVERY CDF boundary separating the two answers,
+  measured in the oracle's float64 CDF -- such mismatches are excused and
+  counted (``Report.excused``); any other mismatch fails;
 * tile mass Z_tile / Z within 1e-3 relative (both below 1e-6 where the
   oracle's mass is under 1e-30);
 * out within 2e-3 absolute; where excused mismatches occurred, against the
@@ -22,6 +23,10 @@ from . import cdf, exact_head, flash_head, gather_mean, logits, prop_head, sampl
 IDX_REL = 1e-5
 MASS_REL = 1e-3
 OUT_ABS = 2e-3
+# Excused mismatches are rare by construction (a threshold must fall within
+# rounding of a boundary); a run that excuses more than this fraction of its
+# samples points at a kernel whose CDF drifts, not at rounding.
+EXCUSED_FRACTION = 0.01
 
 
 @dataclass
@@ -43,9 +48,23 @@ class Report:
         return self
 
 
-def _excused(F: np.ndarray, t: float, a: int, b: int) -> bool:
+def excused_within_bound(rep: "Report") -> bool:
+    """At most EXCUSED_FRACTION of the samples excused (two allowed in any run)."""
+    return rep.excused <= max(2, EXCUSED_FRACTION * rep.samples)
+
+
+def excused(F: np.ndarray, t: float, a: int, b: int) -> bool:
+    """May a sampler return key a where the float64 inverse CDF returns key b?
+
+    Only if float rounding of the CDF can explain it: the two answers differ by
+    crossing the boundaries F(i), i in [min(a, b), max(a, b)), and every one of
+    them must lie within IDX_REL (relative) of the threshold t.  F is
+    non-decreasing, so the farthest boundary is the one at min(a, b) when a < b
+    and at max(a, b) - 1 when a > b; checking all of them covers both."""
     lo, hi = min(a, b), max(a, b)
-    return bool(np.min(np.abs(F[lo:hi] - t)) <= IDX_REL * t)
+    if lo == hi:
+        return True
+    return bool(np.max(np.abs(F[lo:hi] - t)) <= IDX_REL * t)
 
 
 def _check_masses(gpu_m, gpu_z, ref_mass, what, rep):
@@ -80,7 +99,7 @@ def check_prop_head(q, K, V, S, U, tile, gpu_out, gpu_idx, gpu_count=None, gpu_m
         t = float(U) + np.arange(S, dtype=np.float64) / S
         bad = np.nonzero(idx != ref.J)[0]
         for m in bad:
-            assert _excused(ref.F, t[m], int(idx[m]), int(ref.J[m])), (
+            assert excused(ref.F, t[m], int(idx[m]), int(ref.J[m])), (
                 f"{what}: sample {m} picked {idx[m]}, oracle {ref.J[m]}, threshold {t[m]!r}")
         rep.excused += bad.size
         if gpu_count is not None:
@@ -128,7 +147,7 @@ def check_flash_head(q, K, V, S, U, tile, gpu_out, gpu_idx=None, gpu_m=None, gpu
                 e = np.exp(x[k0:k1] - x[k0:k1].max())
                 Ft = cdf(e / e.sum())
                 for s in bad:
-                    assert _excused(Ft, tt[s], int(idx[ti, s]) - k0, int(ref.J[ti, s]) - k0), (
+                    assert excused(Ft, tt[s], int(idx[ti, s]) - k0, int(ref.J[ti, s]) - k0), (
                         f"{what}: tile {ti} sample {s} picked {idx[ti, s]}, oracle {ref.J[ti, s]}")
                 rep.excused += bad.size
             tile_est[ti] = gather_mean(idx[ti], V)
@@ -176,7 +195,7 @@ def check_sampled_head(mode, q, K, V, u, gpu_out, gpu_idx, what=None) -> Report:
     F = cdf(softmax(logits(q, K)))
     bad = np.nonzero(idx != J)[0]
     for m in bad:
-        assert _excused(F, t[m], int(idx[m]), int(J[m])), (
+        assert excused(F, t[m], int(idx[m]), int(J[m])), (
             f"{what}: sample {m} picked {idx[m]}, oracle {J[m]}, threshold {t[m]!r}")
     rep.excused += bad.size
     expect = ref_out if bad.size == 0 else gather_mean(idx, V)

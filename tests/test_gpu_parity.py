@@ -61,6 +61,9 @@ EDGE = [
     ("bf16", 64, 8, 8, 1024, 2048, (3000, 1024, 1)),
     ("bf16", 128, 2, 1, 512, 5000, (600, 40)),
     ("f32", 64, 8, 4, 32, 16, (31, 32, 33)),
+    # bf16 with G = 8: all eight tensor-core B columns and all four t lanes carry live heads
+    ("bf16", 128, 64, 8, 256, 128, (4096, 1000, 0, 777)),
+    ("bf16", 64, 16, 2, 128, 64, (3000, 31, 2049)),
 ]
 
 
@@ -79,6 +82,9 @@ def test_edge_shapes(case, mode):
         U = torch.from_numpy(inp.U[ui]).cuda()
         res = run(inp, mode, dev_inputs=dev[:4] + (U,))
         _report(f"edge{case}/{mode}/U{ui}", check(inp, mode, res, U_index=ui))
+        # the call without debug outputs (the configuration the benchmark times)
+        plain = run(inp, mode, dev_inputs=dev[:4] + (U,), debug=False)
+        assert np.array_equal(plain["out"], res["out"]), "debug outputs changed the result"
 
 
 def test_one_hot_returns_the_row_exactly():
@@ -121,9 +127,15 @@ def test_llama8b_32k_batch1(llama8b_layer, mode, S):
         res = run(inp, mode, S=S, dev_inputs=dev[:4] + (torch.from_numpy(U).cuda(),))
         rep = check(inp, mode, res, S=S, U_values=U)
     else:
+        U = inp.U[0]
         res = run(inp, mode, dev_inputs=dev)
         rep = check(inp, mode, res)
     _report(f"llama8b_32k_b1/{mode}/S{S}", rep)
+    # the call the benchmark times passes no debug struct: it must give the very
+    # same bits as the checked call
+    plain = run(inp, mode, S=S or None, dev_inputs=dev[:4] + (torch.from_numpy(np.ascontiguousarray(U)).cuda(),),
+                debug=False)
+    assert np.array_equal(plain["out"], res["out"]), "debug outputs changed the result"
 
 
 def test_prop_is_deterministic(llama8b_layer):

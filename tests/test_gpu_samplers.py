@@ -39,6 +39,8 @@ def _run_check(inp, mode, S, seed, heads=None):
     u = _uniforms(inp, S, seed)
     res = run(inp, mode, S=S, dev_inputs=dev[:4] + (torch.from_numpy(u).cuda(),))
     rep = check(inp, mode, res, S=S, heads=heads, U_values=u)
+    plain = run(inp, mode, S=S, dev_inputs=dev[:4] + (torch.from_numpy(u).cuda(),), debug=False)
+    assert np.array_equal(plain["out"], res["out"]), "debug outputs changed the result"
     print(f"[parity] {inp.workload.name}/{mode} S={S}: heads={rep.heads} samples={rep.samples} "
           f"excused={rep.excused} max_out_err={rep.max_out_err:.2e}")
     return rep
@@ -56,6 +58,8 @@ EDGE = [
     ("bf16", 128, 8, 2, 32, 7, (0, 1, 33, 300, 2500)),
     ("f32", 64, 4, 4, 64, 1, (5, 64, 65, 700)),
     ("bf16", 64, 16, 2, 1024, 300, (1, 2049, 4096)),
+    ("bf16", 128, 64, 8, 256, 128, (4096, 0, 777)),
+    ("bf16", 64, 16, 2, 128, 64, (3000, 31)),
 ]
 
 
