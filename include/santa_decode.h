@@ -95,7 +95,10 @@ enum { SANTA_MODE_PROP = 0, SANTA_MODE_FLASH = 1, SANTA_MODE_EXACT = 2 };
 enum {
     SANTA_ERR_INDPTR = 1u,   /* kv_indptr entry out of order / range: sequence treated as empty */
     SANTA_ERR_OFFSET = 2u,   /* U outside [0, 1/S) or NaN: clamped into range */
-    SANTA_ERR_TIMEOUT = 4u   /* a bounded wait for an asynchronous copy gave up */
+    SANTA_ERR_TIMEOUT = 4u,  /* a bounded wait gave up (an asynchronous copy, or a
+                                sampler waiting for the scores of its head) */
+    SANTA_ERR_WORKSPACE = 8u /* the workspace held records no pass 1 of this problem
+                                wrote: the affected values were clamped into range */
 };
 
 typedef struct {

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libsanta_decode.so")
 OK, INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA_ERROR, DEVICE_CHECK = range(6)
 F32, BF16 = 0, 1
 MODE_PROP, MODE_FLASH, MODE_EXACT = 0, 1, 2
-ERR_INDPTR, ERR_OFFSET, ERR_TIMEOUT = 1, 2, 4
+ERR_INDPTR, ERR_OFFSET, ERR_TIMEOUT, ERR_WORKSPACE = 1, 2, 4, 8
 
 EXPORTS = (
     "santa_workspace_size",

@@ -405,7 +405,7 @@ __device__ __forceinline__ float checked_offset(const Params &p, float u) {
     return u;
 }
 __device__ __forceinline__ float load_offset(const Params &p, int b, int h) {
-    return checked_offset(p, p.U[b * p.Hq + h]);
+    return checked_offset(p, p.U[size_t(b) * p.Hq + h]);
 }
 
 }  // namespace santa

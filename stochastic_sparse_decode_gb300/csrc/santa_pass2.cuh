@@ -441,7 +441,13 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
         for (int c0 = cw0; c0 < cw1; c0 += kP2Batch) {
             const int kend = min(kP2Batch, cw1 - c0);
             // samples of the batch's chunks: lane k < kend holds chunk k's count
-            const int my_cnt = lane < kend ? sN[c0 - c_lo + lane + 1] - sN[c0 - c_lo + lane] : 0;
+            // N is non-decreasing whenever the records are what pass 1 writes; on any other
+            // workspace a count could come out negative: clamp it and flag the workspace.
+            int my_cnt = lane < kend ? sN[c0 - c_lo + lane + 1] - sN[c0 - c_lo + lane] : 0;
+            if (my_cnt < 0) {
+                raise_flag(p, SANTA_ERR_WORKSPACE);
+                my_cnt = 0;
+            }
             if (c0 > cw0) {  // later batches: read only the chunks that hold a threshold
 #pragma unroll
                 for (int k = 0; k < kP2Batch; ++k) {
@@ -487,7 +493,11 @@ __global__ void __launch_bounds__(kPass2Warps * 32, 2) prop_pass2_kernel(const P
                     for (int s = kP2Batch / 2; s > 0; s >>= 1)
                         if (wcum[k + s - 1] <= g) k += s;
                     const int c = c0 + k, i = c - c_lo;
-                    const int m = sN[i] + g - (k > 0 ? wcum[k - 1] : 0);
+                    int m = sN[i] + g - (k > 0 ? wcum[k - 1] : 0);
+                    if (m >= p.S) {  // only on a workspace pass 1 did not fill (flagged)
+                        raise_flag(p, SANTA_ERR_WORKSPACE);
+                        m = p.S - 1;
+                    }
                     float thr;  // threshold m of the sampler
                     if constexpr (SAMPLER == kSys)
                         thr = fmaf(float(m), invS, u);

@@ -60,3 +60,38 @@ def test_pass1_then_pass2_matches_whole_call(name):
         assert torch.equal(b1[key], b2[key]), key
     for key in ("tile_m", "tile_z"):
         assert torch.equal(torch.nan_to_num(b1[key], nan=-7.0), torch.nan_to_num(b2[key], nan=-7.0)), key
+
+
+def test_pass2_on_a_workspace_pass1_did_not_fill_is_clamped_not_faulted():
+    """santa_prop_pass2 on chunk records and a stash holding NaN, +-inf, negative and
+    huge values: every index it derives stays in range (counts clamped to be
+    non-negative, sample numbers to [0, S)), the output is finite, and a clamp
+    that fired raises SANTA_ERR_WORKSPACE."""
+    import stochastic_sparse_decode_gb300 as sd
+
+    w = Workload(name="passes_garbage", config=42, batch=3, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                 tile=64, S=50, dtype="bf16", lengths=(2500, 0, 700))
+    inp = generate(w)
+    dec = decoder_for(inp)
+    q, k, v, indptr, U = to_torch(inp)
+    ws = dec.workspace("prop").view(torch.float32)
+    # the stash (and anything else): NaN, +-inf, huge, negative and tiny values
+    g = torch.Generator(device="cpu").manual_seed(7)
+    vals = torch.tensor([float("nan"), float("inf"), -float("inf"), -1.0e30, 3.0e38, -7.0, 0.0, 1.0, 1e-30])
+    ws[:] = vals[torch.randint(0, vals.numel(), (ws.numel(),), generator=g)].cuda()
+    # the chunk records (m, z): m = 0 everywhere and z alternating +20 / -19, so the
+    # masses' running sum goes up and down and the threshold counts cannot all be
+    # non-negative -- a clamp must fire
+    nrec = w.batch * w.num_q_heads * (-(-max(w.lengths) // 32))
+    zoff = -(-nrec * 4 // 256) * 256 // 4
+    ws[:nrec] = 0.0
+    ws[zoff : zoff + nrec] = torch.where(torch.arange(nrec, device="cuda") % 2 == 0, 20.0, -19.0)
+    dbg, bufs = dec.debug_buffers("prop")
+    out = dec.pass2(v, indptr, U, debug=dbg)
+    flags = sd.santa_read_device_error(bufs["error_flags"])
+    assert torch.isfinite(out).all()
+    assert flags & sd.ERR_WORKSPACE, f"flags {flags:#x}"
+    idx = bufs["sample_idx"].cpu().numpy()
+    for b, L in enumerate(inp.lengths):
+        sel = idx[b][idx[b] >= 0]
+        assert sel.size == 0 or (sel.min() >= 0 and sel.max() < max(int(L), 1))
