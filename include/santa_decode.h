@@ -50,10 +50,14 @@
  *
  * Ownership: every buffer belongs to the caller.  The library allocates no
  * device memory on the call path; its scratch lives in `workspace` (device,
- * 256-byte aligned, at least santa_workspace_size() bytes), which carries no
- * state from one call to the next.  Calls are asynchronous on `stream`; results
- * are valid once the stream has reached the call's end.  Two calls may run
- * concurrently only with distinct workspaces and outputs.
+ * 256-byte aligned, at least santa_workspace_size() bytes).  The flash and exact
+ * workspaces carry no state from one call to the next.  A prop workspace must be
+ * zero-filled once before its first use (santa_workspace_init, or memory that is
+ * allocated zeroed): its first bytes hold the chunk records through which the
+ * samplers learn that pass 1 has finished a chunk, and every call leaves them
+ * zero again.  Calls are asynchronous on `stream`; results are valid once the
+ * stream has reached the call's end.  Two calls may run concurrently only with
+ * distinct workspaces and outputs.
  *
  * Errors: host-side validation returns a status before anything is enqueued
  * (nothing is written).  Inconsistent device data (a bad kv_indptr entry, an
@@ -129,8 +133,15 @@ typedef struct {
     int sample_stride;       /* flash only: row length of sample_idx */
     unsigned int *error_flags;   /* device word; kernels OR SANTA_ERR_* bits into it */
     santa_event_t main_begin;    /* recorded on `stream` right before / after the */
-    santa_event_t main_end;      /* mode's dominant kernel (prop pass 1, flash tile,
+    santa_event_t main_end;      /* mode's dominant kernel (prop: the fused kernel, or
+                                    pass 1 when the passes run apart; flash tile;
                                     exact stream), for timing that kernel alone */
+    long long wait_cycles;       /* > 0: bound, in SM clock cycles, on a prop sampler's
+                                    wait for its head's scores (0: about 1 s); a wait
+                                    that runs out raises SANTA_ERR_TIMEOUT.  < 0, a
+                                    test of that path: each sampler waits |wait_cycles|
+                                    for one chunk more than its head has, which never
+                                    comes, and gives up */
 } santa_debug;
 
 /*
@@ -140,15 +151,33 @@ typedef struct {
 int santa_workspace_size(const santa_problem *p, int mode, size_t *bytes);
 
 /*
+ * Makes `workspace` ready for the first call of `mode` on problem *p: enqueues on
+ * `stream` a zero fill of the bytes that must start at zero (for prop, the
+ * header and the chunk records; nothing for the other modes).  Needed once per
+ * workspace -- every prop call leaves those bytes zero again -- and again after
+ * a call raised SANTA_ERR_TIMEOUT (which leaves the workspace poisoned: later
+ * calls write zeros and raise SANTA_ERR_WORKSPACE until it is re-initialised).
+ * Returns SANTA_OK, SANTA_INVALID_ARG, SANTA_WORKSPACE_TOO_SMALL or
+ * SANTA_CUDA_ERROR.
+ */
+int santa_workspace_init(const santa_problem *p, int mode, void *workspace, size_t workspace_bytes,
+                         santa_stream_t stream);
+
+/*
  * S2ANTA-prop decode (paper notes, Key designs 1-2).
  * q, k, v, kv_indptr, U, out, workspace: device pointers as described above.
- * Two kernels on `stream`: pass 1 (scores, stash, one record per 32-key chunk)
- * and pass 2 (reducer over the ceil(L_b / 32) chunk records, per-chunk
- * systematic search, V gather, deterministic combine).  Workspace: the chunk
- * records, 2 x [B][Hq][ceil(max_len / 32)] float32, and the score stash
- * [B][Hq][max_len] float32.  Supported up to max_len of about 4 million keys
- * (pass 2 keeps its share of the chunk records in shared memory; longer is
- * SANTA_UNSUPPORTED).  Returns a status; see the conventions above.
+ * One persistent kernel on `stream`, one CTA per SM, all resident at once: its
+ * streaming warps are pass 1 (scores, stash, one record per 32-key chunk) and
+ * its sampler warps are pass 2, one head at a time (reducer over the
+ * ceil(L_b / 32) chunk records, per-chunk systematic search, V gather,
+ * deterministic combine), each head starting as soon as its records are all
+ * written.  When the fused kernel's shared memory does not fit (stratified or
+ * i.i.d. samplers with large S), the same two stages run as two kernels.
+ * Workspace: a 256-byte header, the chunk records [B][Hq][ceil(max_len / 32)]
+ * as 64-bit words, and the score stash [B][Hq][32 ceil(max_len / 32)] float32; zero-filled
+ * once before first use (see santa_workspace_init).  Supported up to
+ * max_len = 2^22 keys (longer is SANTA_UNSUPPORTED).  Returns a status; see the
+ * conventions above.
  */
 int santa_decode_prop(const santa_problem *p, const void *q, const void *k, const void *v,
                       const long long *kv_indptr, const float *U, float *out,
@@ -167,10 +196,14 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
  *                     of dbg it uses error_flags, main_begin and main_end.
  *   santa_prop_pass2  reads the workspace as santa_prop_pass1 left it for the
  *                     same problem, V, kv_indptr and the offsets U; writes out
- *                     and dbg's tile and sample outputs.  It must follow
- *                     santa_prop_pass1 on the same problem and workspace in
- *                     stream order: on a workspace that pass 1 did not fill, the
- *                     chunk records are arbitrary and the behaviour is undefined.
+ *                     and dbg's tile and sample outputs, and sets the chunk
+ *                     records back to zero (the workspace is then ready for any
+ *                     prop call).  It follows santa_prop_pass1 on the same problem
+ *                     and workspace in stream order.  On any other workspace the
+ *                     records are whatever it holds: every index derived from them
+ *                     is clamped into range (no out-of-bounds access), a record
+ *                     that reads zero counts as a chunk without mass, `out` stays
+ *                     finite, and SANTA_ERR_WORKSPACE is raised where a clamp fired.
  *
  * Arguments, ownership and errors are those of santa_decode_prop; a pass takes
  * only the pointers it reads.
@@ -280,10 +313,16 @@ int exact_decode(const santa_problem *p, const void *q, const void *k, const voi
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Every call shares the one array, which keeps the last
- * call's contents; no scratch value has to start at zero (each call writes every
- * value before reading it), so results never depend on an earlier call.  Calls whose kernels overlap on the GPU
- * (unordered streams or threads) race on the array: order them.
+ * any stream capture.  (After a device reset the address is looked up again.)
+ * Every call shares the one array, which keeps the last call's contents.  The
+ * part of it that a prop workspace needs zero-filled (santa_workspace_init)
+ * starts zero -- device arrays are zero when the library's code is loaded -- and
+ * every call leaves it zero again; the rest is written before it is read, so
+ * results never depend on an earlier call.  One exception: a call that raises
+ * SANTA_ERR_TIMEOUT (a wait that gave up after about a second) poisons the array,
+ * and later calls write zeros and raise SANTA_ERR_WORKSPACE until the process
+ * exits.  Calls whose kernels overlap on the GPU (unordered streams or threads)
+ * race on the array: order them.
  */
 int santa_decode_prop_static_scratch(const santa_problem *p, const void *q, const void *k, const void *v,
                                      const long long *kv_indptr, const float *U, float *out,

@@ -25,6 +25,7 @@ ERR_INDPTR, ERR_OFFSET, ERR_TIMEOUT, ERR_WORKSPACE = 1, 2, 4, 8
 
 EXPORTS = (
     "santa_workspace_size",
+    "santa_workspace_init",
     "santa_decode_prop",
     "santa_prop_pass1",
     "santa_prop_pass2",
@@ -73,6 +74,7 @@ class Debug(ctypes.Structure):
         ("error_flags", ctypes.c_void_p),
         ("main_begin", ctypes.c_void_p),
         ("main_end", ctypes.c_void_p),
+        ("wait_cycles", ctypes.c_longlong),
     ]
 
 
@@ -103,6 +105,7 @@ def lib() -> ctypes.CDLL:
         vp, sz = ctypes.c_void_p, ctypes.c_size_t
         P, Dp = ctypes.POINTER(Problem), ctypes.POINTER(Debug)
         L.santa_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
+        L.santa_workspace_init.argtypes = [P, ctypes.c_int, vp, sz, vp]
         for name in ("santa_decode_prop", "santa_decode_prop_strat", "santa_decode_prop_iid", "santa_decode_flash"):
             getattr(L, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_prop_pass1.argtypes = [P, vp, vp, vp, vp, sz, Dp, vp]
@@ -136,6 +139,15 @@ def workspace_size(problem: Problem, mode: int) -> int:
     if st != OK:
         raise SantaError(st, "santa_workspace_size")
     return n.value
+
+
+def santa_workspace_init(problem: Problem, mode: int, workspace, stream=None) -> None:
+    """Enqueues the zero fill a workspace needs before its first call (and after a
+    SANTA_ERR_TIMEOUT): see santa_decode.h."""
+    st = lib().santa_workspace_init(ctypes.byref(problem), int(mode), _ptr(workspace), _nbytes(workspace),
+                                    _stream(stream))
+    if st != OK:
+        raise SantaError(st, "santa_workspace_init")
 
 
 def _ptr(t) -> int | None:

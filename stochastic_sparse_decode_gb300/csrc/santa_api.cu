@@ -14,6 +14,7 @@ namespace {
 
 constexpr long long kMaxTokens = (1LL << 31) - 4096;  // TMA row coordinates are int32
 constexpr int kMaxS = 1 << 20;
+constexpr int kMaxPropLen = 1 << 22;  // 2^17 chunks of 32 keys
 
 __global__ void zero_out_kernel(float *out, size_t n) {
     for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
@@ -25,8 +26,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Layout {
-    int Tmax = 0, nch = 0, nsplit = 0, cps = 0;
+    int Tmax = 0, nch = 0;
     size_t rec_m = 0, rec_z = 0, stash = 0, partial = 0, total = 0;
+    size_t cnt = 0, rec = 0, clear = 0;  // prop: counters, packed chunk records; bytes that start at zero
 };
 
 int check_problem(const santa_problem *p, int mode) {
@@ -42,6 +44,8 @@ int check_problem(const santa_problem *p, int mode) {
     if (p->dtype != SANTA_F32 && p->dtype != SANTA_BF16) return SANTA_UNSUPPORTED;
     if (!is_pow2(p->tile) || p->tile < 32 || p->tile > 1024) return SANTA_INVALID_ARG;
     if (mode != SANTA_MODE_EXACT && (p->S < 1 || p->S > kMaxS)) return SANTA_INVALID_ARG;
+    // prop's fixed-point masses hold at most 2^17 chunks of 32 keys per sequence
+    if (mode == SANTA_MODE_PROP && p->max_len > kMaxPropLen) return SANTA_UNSUPPORTED;
     if (p->max_len < 0 || p->total_tokens < 0 || p->total_tokens > kMaxTokens) return SANTA_INVALID_ARG;
     if ((p->max_len + p->tile - 1) / p->tile > 65535) return SANTA_INVALID_ARG;  // tiles are a grid dimension
     return SANTA_OK;
@@ -49,23 +53,16 @@ int check_problem(const santa_problem *p, int mode) {
 
 // Workspace regions of one call, each 256-byte aligned.  Sizes are computed in
 // double first so that absurd shapes are rejected instead of wrapping around.
-//   prop:        chunk records rec_m, rec_z [B][Hq][nch], nch = ceil(max_len / 32),
-//                and the score stash [B][Hq][max_len];
+//   prop:        a 256-byte header (its first word: nonzero = poisoned by a timeout),
+//                per (sequence, query head) the count of chunks pass 1 has published,
+//                the chunk records [B][Hq][nch] as 64-bit words (m, z), nch =
+//                ceil(max_len / 32), and the score stash [B][Hq][nch * 32]; the header
+//                counters and records must be zero before the first call (`clear` bytes
+//                from the start) and every call leaves them so;
 //   flash:       tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d];
 //   exact:       per (sequence, streaming warp, head of the group) the partial state
 //                (M, Z) as rec_m [B][P][G][2] and O as [B][P][G][d], P the warps of
 //                the streaming kernel's largest grid.
-// SMs of the current device (152 on GB300, also the answer without a device).
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        n <= 0) {
-        cudaGetLastError();  // leave no sticky error behind on a machine without a device
-        return 152;
-    }
-    return n;
-}
-
 int make_layout(const santa_problem *p, int mode, Layout *L) {
     const int Tmax = (p->max_len + p->tile - 1) / p->tile;
     const int nch = (p->max_len + 31) / 32;
@@ -89,7 +86,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     const double nrec = B * Hq * (prop ? nch : Tmax);
     double est = 2 * nrec * 4;
     if (prop)
-        est += B * Hq * double(p->max_len) * 4;
+        est += nrec * 32 * 4;
     else
         est += nrec * D * 4;
     if (est > 1e15) return SANTA_INVALID_ARG;
@@ -98,15 +95,20 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     size_t off = 0;
     L->Tmax = Tmax;
     L->nch = nch;
-    prop_split(nch, p->tile, (long long)p->batch * p->num_q_heads, sm_count(), &L->nsplit, &L->cps);
-    L->rec_m = off;
-    off += align256(n_rec * 4);
-    L->rec_z = off;
-    off += align256(n_rec * 4);
     if (prop) {
+        off = 256;  // header
+        L->cnt = off;
+        off += align256(size_t(p->batch) * p->num_q_heads * 4);
+        L->rec = off;
+        off += align256(n_rec * 8);
+        L->clear = off;
         L->stash = off;
-        off += align256(size_t(p->batch) * p->num_q_heads * size_t(p->max_len) * 4);
+        off += align256(n_rec * 32 * 4);
     } else {
+        L->rec_m = off;
+        off += align256(n_rec * 4);
+        L->rec_z = off;
+        off += align256(n_rec * 4);
         L->partial = off;
         off += align256(n_rec * p->head_dim * 4);
     }
@@ -119,10 +121,9 @@ int smem_check(const santa_problem *p, int mode, int sampler, bool paged) {
     const int G = p->num_q_heads / p->num_kv_heads;
     size_t need = 0;
     if (mode == SANTA_MODE_PROP) {
-        Layout L;
-        if (make_layout(p, mode, &L) != SANTA_OK) return SANTA_INVALID_ARG;
+        (void)paged;  // the paged kernels use the same shared memory
         need = prop_pass1_smem(p->dtype, p->head_dim, G, int(kOptin));
-        const size_t s2 = prop_pass2_smem(p->head_dim, L.cps, sampler, p->S, paged);
+        const size_t s2 = prop_sampler_smem(p->head_dim, sampler, p->S);
         if (s2 > need) need = s2;
     } else if (mode == SANTA_MODE_FLASH) {
         need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
@@ -269,12 +270,16 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
     prm.u_samples = sampler == kSys ? nullptr : U;
     prm.sampler = sampler;
     prm.out = out;
-    prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
-    prm.rec_z = reinterpret_cast<float *>(ws + L.rec_z);
-    prm.stash = mode == SANTA_MODE_PROP ? reinterpret_cast<float *>(ws + L.stash) : nullptr;
-    prm.partial = mode == SANTA_MODE_PROP ? nullptr : reinterpret_cast<float *>(ws + L.partial);
-    prm.nsplit = L.nsplit;
-    prm.chunks_per_split = L.cps;
+    if (mode == SANTA_MODE_PROP) {
+        prm.hdr = reinterpret_cast<unsigned int *>(ws);
+        prm.rec = reinterpret_cast<unsigned long long *>(ws + L.rec);
+        prm.cnt = reinterpret_cast<unsigned int *>(ws + L.cnt);
+        prm.stash = reinterpret_cast<float *>(ws + L.stash);
+    } else {
+        prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
+        prm.rec_z = reinterpret_cast<float *>(ws + L.rec_z);
+        prm.partial = reinterpret_cast<float *>(ws + L.partial);
+    }
     Timing tm;
     if (dbg) {
         prm.dbg_tile_m = dbg->tile_m;
@@ -283,6 +288,7 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
         prm.dbg_idx = dbg->sample_idx;
         prm.dbg_stride = dbg->sample_stride;
         prm.err = dbg->error_flags;
+        prm.wait_cycles = dbg->wait_cycles;
         tm.begin = reinterpret_cast<cudaEvent_t>(dbg->main_begin);
         tm.end = reinterpret_cast<cudaEvent_t>(dbg->main_end);
     }
@@ -321,6 +327,21 @@ int santa_workspace_size(const santa_problem *p, int mode, size_t *bytes) {
     if (s2 != SANTA_OK) return s2;
     *bytes = L.total;
     return SANTA_OK;
+}
+
+int santa_workspace_init(const santa_problem *p, int mode, void *workspace, size_t workspace_bytes,
+                         santa_stream_t stream) {
+    const int st = check_problem(p, mode);
+    if (st != SANTA_OK) return st;
+    Layout L;
+    const int s2 = make_layout(p, mode, &L);
+    if (s2 != SANTA_OK) return s2;
+    if (!workspace || !aligned(workspace, 256)) return SANTA_INVALID_ARG;
+    if (workspace_bytes < L.total) return SANTA_WORKSPACE_TOO_SMALL;
+    if (L.clear == 0) return SANTA_OK;
+    return cudaMemsetAsync(workspace, 0, L.clear, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SANTA_OK
+               : SANTA_CUDA_ERROR;
 }
 
 int santa_decode_prop(const santa_problem *p, const void *q, const void *k, const void *v, const long long *kv_indptr,

@@ -17,8 +17,6 @@ namespace santa {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kTileWarps = 4;    // warps of a tile CTA
 constexpr int kWarpRows = 64;    // K/V rows per TMA chunk of one tile-kernel warp (2 per lane)
-constexpr int kPass2Warps = 8;   // warps of a prop pass-2 CTA
-constexpr int kMaxSplit = 8;     // prop pass 2: CTAs per head = size of its cluster
 constexpr int kMergeThreads = 128;
 constexpr int kExactCtaBound = 160;  // exact: streaming CTAs at most (the workspace is sized for it)
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
@@ -43,12 +41,16 @@ struct Params {
     float *out;
     // workspace
     float *rec_m, *rec_z;  // flash: [B][Hq][Tmax] tile max logit and partition sum;
-                           // prop: [B][Hq][nch] the same per 32-key chunk;
                            // exact: rec_m holds float2 (M, Z) per (sequence, warp, head)
-    float *stash;          // prop: [B][Hq][max_len] exp(x - m_c), key i of sequence b at i
+    unsigned long long *rec;  // prop: [B][Hq][nch] chunk records, (m_c, z_c) as one 64-bit
+                              // word, z in the high half; 0 = not written (see store_record)
+    unsigned int *cnt;        // prop: [B][Hq] chunks published to the head's sampler (publish_chunks)
+    unsigned int *hdr;        // prop: workspace header word; nonzero = poisoned by a timeout
+    long long wait_cycles;    // bound on a sampler's wait for its records (0: kWaitCycles)
+    float *stash;          // prop: [B][Hq][nch * 32] exp(x - m_c), key i of sequence b at i
+                           // (rows padded to whole chunks: a chunk's scores are one 128-byte line)
     float *partial;        // flash: [B][Hq][Tmax][D] tile estimates;
                            // exact: [sequence slot][warp][head][D] unnormalised sums
-    int nsplit, chunks_per_split;  // prop pass 2: CTAs (one cluster) per head, chunks per CTA
     int sampler;                   // prop: kSys, kStrat or kIid
     // optional debug outputs
     float *dbg_tile_m, *dbg_tile_z;

@@ -1,7 +1,7 @@
 // santa_exact.cu -- launch of the exact split-KV decode: streaming kernel, then merge.
 #include "santa_exact_stream.cuh"
 #include "santa_launch.h"
-#include "santa_pass2.cuh"
+#include "santa_merge.cuh"
 
 namespace santa {
 
@@ -33,10 +33,10 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
         cudaError_t e = ensure_smem(k1, s1);
         if (e != cudaSuccess) return e;
         record_event(tm.begin, stream);
-        e = launch_kernel(k1, dim3(unsigned(C)), dim3(EG::kWarps * 32), s1, stream, false, 0, kmap, vmap, p);
+        e = launch_kernel(k1, dim3(unsigned(C)), dim3(EG::kWarps * 32), s1, stream, false, 0, false, kmap, vmap, p);
         if (e != cudaSuccess) return e;
         record_event(tm.end, stream);
-        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kExactMergeWarps * 32), 0, stream, false, 0, p, C, int(EG::kWarps));
+        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kExactMergeWarps * 32), 0, stream, false, 0, false, p, C, int(EG::kWarps));
     });
 }
 

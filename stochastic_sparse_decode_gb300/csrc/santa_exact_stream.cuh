@@ -23,7 +23,7 @@
 #pragma once
 
 #include "santa_common.cuh"
-#include "santa_pass2.cuh"
+#include "santa_merge.cuh"
 #include "santa_stream.cuh"
 #include "santa_tile.cuh"
 

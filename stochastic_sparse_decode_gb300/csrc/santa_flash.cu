@@ -1,6 +1,6 @@
 // santa_flash.cu -- launch of S2ANTA-flash: tile kernel then merge.
 #include "santa_launch.h"
-#include "santa_pass2.cuh"
+#include "santa_merge.cuh"
 #include "santa_tile.cuh"
 
 namespace santa {
@@ -19,10 +19,10 @@ cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cu
         cudaError_t e = ensure_smem(k1, s1);
         if (e != cudaSuccess) return e;
         record_event(tm.begin, stream);
-        e = launch_kernel(k1, dim3(p.Hkv, p.Tmax, p.B), dim3(kTileWarps * 32), s1, stream, false, 0, kmap, p);
+        e = launch_kernel(k1, dim3(p.Hkv, p.Tmax, p.B), dim3(kTileWarps * 32), s1, stream, false, 0, false, kmap, p);
         if (e != cudaSuccess) return e;
         record_event(tm.end, stream);
-        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, true, 0, p);
+        return launch_kernel(k2, dim3(p.Hq, p.B), dim3(kMergeThreads), 0, stream, true, 0, false, p);
     });
 }
 

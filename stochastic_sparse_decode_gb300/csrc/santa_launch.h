@@ -10,26 +10,6 @@
 
 namespace santa {
 
-// prop pass 2: CTAs per head (a cluster of at most kMaxSplit) and 32-key chunks
-// per CTA -- whole tiles (so a tile's debug totals stay in one CTA) and a
-// multiple of the warp count.  About 128 chunks (16 per warp) per CTA while the
-// heads are too few to fill the GPU; with `heads` (batch x query heads) enough for
-// two CTAs per SM on their own, fewer splits, because every split re-runs the
-// head's reducer.  At most 8192 chunks per CTA (their records sit in shared memory).
-inline void prop_split(int nch, int tile, long long heads, int sms, int *nsplit, int *cps) {
-    const int unit = (tile / 32) > kPass2Warps ? tile / 32 : kPass2Warps;
-    int n = (nch + 127) / 128;
-    const long long fill = heads > 0 ? (2LL * sms + heads - 1) / heads : 1;  // splits for two CTAs per SM
-    if (n > fill) n = int(fill);
-    const int n_smem = (nch + 8191) / 8192;
-    if (n < n_smem) n = n_smem;
-    n = n < 1 ? 1 : (n > kMaxSplit ? kMaxSplit : n);
-    int per = (nch + n - 1) / n;
-    per = (per + unit - 1) / unit * unit;
-    *nsplit = n;
-    *cps = per < unit ? unit : per;
-}
-
 // Records the timing event `ev` (if any) on `stream`.  Inside stream capture it
 // becomes an event-record node of the graph, so a replayed graph is timed too.
 inline void record_event(cudaEvent_t ev, cudaStream_t stream) {
@@ -44,15 +24,17 @@ inline void record_event(cudaEvent_t ev, cudaStream_t stream) {
 // Launches `kern` on `stream`; with `pdl` the kernel may start while the
 // previous kernel in the stream drains (programmatic dependent launch).
 // With cluster_x > 0 the grid's x dimension is cut into thread-block clusters of that size.
+// With `cooperative` every CTA of the grid is resident at once (the launch fails
+// rather than run a grid that cannot be).
 template <typename... Exp, typename... Act>
 cudaError_t launch_kernel(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
-                          int cluster_x, Act &&...args) {
+                          int cluster_x, bool cooperative, Act &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     int n = 0;
     if (pdl) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -64,6 +46,11 @@ cudaError_t launch_kernel(void (*kern)(Exp...), dim3 grid, dim3 block, size_t sm
         attr[n].val.clusterDim.x = unsigned(cluster_x);
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
         ++n;
     }
     cfg.attrs = n ? attr : nullptr;
@@ -101,7 +88,8 @@ struct Timing {
 
 // Mode launchers (one translation unit each).  `dtype` is SANTA_F32/SANTA_BF16.
 // kmap32: the K descriptor with boxes of 32 rows (the streaming pass-1 kernel).
-// stages: kPass1 | kPass2 (santa_decode_prop runs both, in that order).
+// stages: kPass1 | kPass2 (santa_decode_prop runs both: in one fused kernel when
+// its shared memory fits, else as two kernels in that order).
 enum { kPass1 = 1, kPass2 = 2 };
 cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm,
                         int stages);
@@ -111,7 +99,8 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
 
 // Shared-memory needs, for validation on the host.
 size_t prop_pass1_smem(int dtype, int D, int G, int smem_optin);
-size_t prop_pass2_smem(int D, int cps, int sampler, int S, bool paged);
+size_t prop_sampler_smem(int D, int sampler, int S);
+size_t prop_fused_smem(int dtype, int D, int G, int sampler, int S, int smem_optin, int *nbuf);
 size_t flash_tile_smem(int dtype, int D, int G, int tile);
 size_t exact_stream_smem(int dtype, int D, int G);
 int exact_stream_warps(int dtype, int D, int G);

@@ -1,6 +1,7 @@
-// santa_prop.cu -- launch of S2ANTA-prop: the streaming pass 1, then pass 2.
+// santa_prop.cu -- launch of S2ANTA-prop: the fused persistent kernel (pass 1 and
+// the samplers in one grid), or pass 1 and the sampler as two kernels.
 #include "santa_launch.h"
-#include "santa_pass2.cuh"
+#include "santa_sampler.cuh"
 #include "santa_stream.cuh"
 
 namespace santa {
@@ -18,18 +19,45 @@ size_t prop_pass1_smem(int dtype, int d, int g, int smem_optin) {
     return bytes;
 }
 
-size_t prop_pass2_smem(int d, int cps, int sampler, int S, bool paged) {
+// The sampler alone: one CTA per (sequence, query head).
+size_t prop_sampler_smem(int d, int sampler, int S) {
     const int nu = sampler_slots(sampler, S);
-    return d == 128 ? Pass2Smem<uint16_t, 128>::bytes(cps, nu, paged) : Pass2Smem<uint16_t, 64>::bytes(cps, nu, paged);
+    return d == 128 ? SampSmem<128>::bytes(nu) : SampSmem<64>::bytes(nu);
+}
+
+// The fused kernel: the streaming layout with as many buffers per warp as fit,
+// which the samplers then reuse; 0 if it does not fit.  *nbuf: the buffers per warp.
+size_t prop_fused_smem(int dtype, int d, int g, int sampler, int S, int smem_optin, int *nbuf) {
+    size_t bytes = 0;
+    SANTA_DISPATCH(dtype, d, g, {
+        using CG = ChunkGeom<T, D, G>;
+        const int nb = CG::nbuf_for(size_t(smem_optin));
+        const size_t need = nb ? fused_smem_bytes<T, D, G>(nb, sampler_slots(sampler, S)) : size_t(-1);
+        bytes = need <= size_t(smem_optin) ? need : 0;
+        if (nbuf) *nbuf = nb;
+        return cudaSuccess;
+    });
+    return bytes;
+}
+
+template <typename T, int D, int G>
+static void *fused_for(int sampler, bool paged) {
+    if (paged) return sampler == kSys ? reinterpret_cast<void *>(prop_fused_kernel<T, D, G, kSys, true>) : nullptr;
+    switch (sampler) {
+        case kSys: return reinterpret_cast<void *>(prop_fused_kernel<T, D, G, kSys, false>);
+        case kStrat: return reinterpret_cast<void *>(prop_fused_kernel<T, D, G, kStrat, false>);
+        case kIid: return reinterpret_cast<void *>(prop_fused_kernel<T, D, G, kIid, false>);
+        default: return nullptr;
+    }
 }
 
 template <typename T, int D>
-static void *pass2_for(int sampler, bool paged) {
-    if (paged) return sampler == kSys ? reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys, true>) : nullptr;
+static void *sampler_for(int sampler, bool paged) {
+    if (paged) return sampler == kSys ? reinterpret_cast<void *>(prop_sample_kernel<T, D, kSys, true>) : nullptr;
     switch (sampler) {
-        case kSys: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys, false>);
-        case kStrat: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kStrat, false>);
-        case kIid: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kIid, false>);
+        case kSys: return reinterpret_cast<void *>(prop_sample_kernel<T, D, kSys, false>);
+        case kStrat: return reinterpret_cast<void *>(prop_sample_kernel<T, D, kStrat, false>);
+        case kIid: return reinterpret_cast<void *>(prop_sample_kernel<T, D, kIid, false>);
         default: return nullptr;
     }
 }
@@ -59,36 +87,66 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
     int sms = 0, optin = 0;
     cudaError_t e0 = device_limits(&sms, &optin);
     if (e0 != cudaSuccess) return e0;
+    const bool paged = p.page_table != nullptr;
     return SANTA_DISPATCH(dtype, p.D, p.G, {
         using CG = ChunkGeom<T, D, G>;
-        const int nbuf = CG::nbuf_for(size_t(optin));
-        if (!nbuf) return cudaErrorNotSupported;
-        auto k1 = p.page_table ? prop_stream_kernel<T, D, G, true> : prop_stream_kernel<T, D, G, false>;
-        const size_t s1 = CG::bytes(nbuf);
-        auto k2 = reinterpret_cast<void (*)(const Params)>(pass2_for<T, D>(p.sampler, p.page_table != nullptr));
-        if (!k2) return cudaErrorInvalidValue;
-        const size_t s2 = Pass2Smem<T, D>::bytes(p.chunks_per_split, sampler_slots(p.sampler, p.S), p.page_table);
-        cudaError_t e = ensure_smem(k1, s1);
-        if (e == cudaSuccess) e = ensure_smem(k2, s2);
-        if (e != cudaSuccess) return e;
         // One CTA per SM, a multiple of Hkv CTAs so that every warp keeps one KV head;
         // no more CTAs than a warp each of chunks.
         const long long chunks = (long long)p.B * p.nch * p.Hkv;
         long long grid = sms >= p.Hkv ? (long long)(sms / p.Hkv) * p.Hkv : sms;
         if (grid > chunks) grid = chunks;
-        if (stages & kPass1) record_event(tm.begin, stream);
-        // Pass 1 may launch early (programmatic dependent launch): behind a previous
-        // call's pass 2 it sets up while that kernel drains.  Pass 2 goes in plain
-        // stream order -- launched early, its CTAs only wait on SMs pass 1 is using
-        // (measured on GB300: 25.3 us per layer-step this way, 26.6 with neither
-        // kernel early, 29.4 with both, 30.8 with only pass 2).
+        int nbf = 0;
+        size_t sf = prop_fused_smem(dtype, D, G, p.sampler, p.S, optin, &nbf);
+        cudaError_t e = cudaSuccess;
+        auto kf = reinterpret_cast<void (*)(const CUtensorMap, const Params, int)>(fused_for<T, D, G>(p.sampler, paged));
+        if (!kf) return cudaErrorInvalidValue;
+        if ((stages & kPass1) && (stages & kPass2) && sf) {
+            e = ensure_smem(kf, sf);
+            if (e != cudaSuccess) return e;
+            // every CTA of the grid must fit on the device at once
+            int per_sm = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kf, kChunkWarps * 32, sf);
+            if (e != cudaSuccess) return e;
+            if ((long long)per_sm * sms < grid) sf = 0;  // not resident at once: two kernels
+        }
+        if ((stages & kPass1) && (stages & kPass2) && sf) {
+            // The fused kernel: every CTA resident at once (cooperative launch), since
+            // a sampler waits for records that other CTAs write; launched early behind
+            // the previous kernel (programmatic dependent launch), whose completion it
+            // awaits before touching global memory.
+            record_event(tm.begin, stream);
+            e = launch_kernel(kf, dim3(unsigned(grid)), dim3(kChunkWarps * 32), sf, stream, true, 0, true, kmap32, p,
+                              nbf);
+            if (e != cudaSuccess) {  // without the early launch if the two attributes do not combine
+                cudaGetLastError();
+                e = launch_kernel(kf, dim3(unsigned(grid)), dim3(kChunkWarps * 32), sf, stream, false, 0, true, kmap32,
+                                  p, nbf);
+            }
+            if (e != cudaSuccess) return e;
+            record_event(tm.end, stream);
+            return cudaSuccess;
+        }
         if (stages & kPass1) {
-            e = launch_kernel(k1, dim3(unsigned(grid)), dim3(kChunkWarps * 32), s1, stream, true, 0, kmap32, p, nbuf);
+            const int nbuf = CG::nbuf_for(size_t(optin));
+            if (!nbuf) return cudaErrorNotSupported;
+            auto k1 = paged ? prop_stream_kernel<T, D, G, true> : prop_stream_kernel<T, D, G, false>;
+            const size_t s1 = CG::bytes(nbuf);
+            e = ensure_smem(k1, s1);
+            if (e != cudaSuccess) return e;
+            record_event(tm.begin, stream);
+            e = launch_kernel(k1, dim3(unsigned(grid)), dim3(kChunkWarps * 32), s1, stream, true, 0, false, kmap32, p,
+                              nbuf);
             if (e != cudaSuccess) return e;
             record_event(tm.end, stream);
         }
         if (!(stages & kPass2)) return cudaSuccess;
-        return launch_kernel(k2, dim3(p.nsplit, p.Hq, p.B), dim3(kPass2Warps * 32), s2, stream, false, p.nsplit, p);
+        auto k2 = reinterpret_cast<void (*)(const Params)>(sampler_for<T, D>(p.sampler, paged));
+        if (!k2) return cudaErrorInvalidValue;
+        const size_t s2 = prop_sampler_smem(D, p.sampler, p.S);
+        e = ensure_smem(k2, s2);
+        if (e != cudaSuccess) return e;
+        const long long items = (long long)p.B * p.Hq;
+        return launch_kernel(k2, dim3(unsigned(items)), dim3(kSampThreads), s2, stream, false, 0, false, p);
     });
 }
 

@@ -10,11 +10,12 @@
 //
 // The entry point runs the same kernels as santa_decode_prop, with this array
 // as their workspace; it allocates nothing itself and calls no allocating
-// routine.  All calls share the array and it keeps the last call's contents;
-// nothing in it has to start at zero -- every call writes each scratch value
-// before reading it -- so a call never depends on what an earlier call left
-// behind.  Calls whose kernels overlap on the GPU (different streams, or
-// threads that do not order their streams) race on the array.
+// routine.  All calls share the array and it keeps the last call's contents.
+// The bytes a prop workspace needs zero-filled start zero (a __device__ array is
+// zero when the module is loaded) and every call leaves them zero; everything
+// else is written before it is read, so a call never depends on what an earlier
+// call left behind.  Calls whose kernels overlap on the GPU (different streams,
+// or threads that do not order their streams) race on the array.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>

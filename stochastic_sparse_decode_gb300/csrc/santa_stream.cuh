@@ -50,10 +50,11 @@ constexpr int kChunkWarps = 12;                     // warps of a pass-1 CTA
 constexpr int kChunkMaxBuf = 4;                     // buffers per warp, at most
 constexpr int kChunkBoxBytes = kChunkRows * 128;    // one TMA box: 32 rows x 128 bytes
 
-// What a buffer holds: chunk ch of sequence b (rows start + 32 ch ..), KV head, keys.
+// What a buffer holds: chunk ch of sequence b (rows start + 32 ch ..), KV head, keys,
+// and whether the chunk has records (its keys, or a page dropped for a bad id).
 struct ChunkSlot {
     long long start;
-    int b, ch, kvh, len;
+    int b, ch, kvh, len, rec;
 };
 
 template <typename T, int D, int G>
@@ -179,9 +180,61 @@ __device__ __forceinline__ void chunk_logits_mma(const unsigned char *base, cons
         for (int mt = 0; mt < 2; ++mt) mma_bf16_16816(c[mt], a[mt][ks], qf[ks]);
 }
 
+// Shared memory of the streaming warps, from a 1024-byte aligned base: [kChunkWarps][nbuf]
+// chunk buffers, then per warp kChunkMaxBuf mbarriers and slot descriptors, then the
+// CTA's claim counter.  Initialised by stream_setup, used by stream_chunks.
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+    return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Barrier and counter initialisation of the streaming warps (warps 0 .. kChunkWarps - 1);
+// the caller makes it visible with a CTA barrier before stream_chunks.
+template <typename T, int D, int G>
+__device__ __forceinline__ void stream_setup(const CUtensorMap &kmap, unsigned char *smem, int nbuf) {
+    using CG = ChunkGeom<T, D, G>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < kChunkWarps && lane < nbuf)
+        mbar_init(reinterpret_cast<uint64_t *>(smem + CG::bars_off(nbuf)) + warp * kChunkMaxBuf + lane, 1);
+    if (threadIdx.x == 0) {
+        *reinterpret_cast<int *>(smem + CG::next_off(nbuf)) = 0;
+        prefetch_tensormap(&kmap);
+    }
+    fence_barrier_init();
+}
+
+// Stores the partition record (m_c, z_c) of one chunk and query head as one 64-bit
+// word, z in the high half (a single store, so a reader sees both halves of one
+// record or neither).  A written word is never 0 -- z >= 1 (the chunk's largest key
+// contributes exp(0) = 1) or NaN, and a chunk dropped for a bad page id carries
+// m = -inf -- so 0 means "not written yet".
+__device__ __forceinline__ void store_record(unsigned long long *rec, float m, float z) {
+    const unsigned long long v = (static_cast<unsigned long long>(__float_as_uint(z)) << 32) | __float_as_uint(m);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(rec), "l"(v) : "memory");
+}
+
+// Publishes n finished chunks of KV head kvh of sequence b to the samplers of the
+// group's G query heads: a fence that makes the warp's stash and record stores
+// visible (every lane's stores precede the publishing lanes' fences through the
+// warp barrier), then count[b][h] += n for each head h of the group.  A warp
+// publishes when it leaves a (sequence, KV head) and at the end of its walk, not
+// per chunk: a fence waits for the warp's stores to land, which under a saturated
+// memory system costs about a microsecond of the warp's time.
+template <int G>
+__device__ __forceinline__ void publish_chunks(const Params &p, int b, int kvh, int n, int lane) {
+    __syncwarp();
+    if (lane < G) {
+        __threadfence();
+        atomicAdd(p.cnt + size_t(b) * p.Hq + kvh * G + lane, unsigned(n));
+    }
+    __syncwarp();
+}
+
+// The streaming walk of pass 1, run by warps 0 .. kChunkWarps - 1 of a CTA whose
+// shared memory `smem` (1024-byte aligned) holds the streaming layout, after
+// stream_setup, a CTA barrier and the kernel's dependency wait.  Returns whether a
+// wait for one of the warp's copies timed out (after a bounded wait for the rest).
 template <typename T, int D, int G, bool kPaged>
-__global__ void __launch_bounds__(kChunkWarps * 32, 1)
-    prop_stream_kernel(const __grid_constant__ CUtensorMap kmap, const Params p, int nbuf) {
+__device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Params &p, int nbuf, unsigned char *smem) {
     using Geo = TileGeom<T, D>;
     using CG = ChunkGeom<T, D, G>;
     constexpr int kGH = CG::kGH, kVPL = CG::kVPL, kKB = CG::kKB, kPairs = Geo::kPairs;
@@ -194,27 +247,10 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     const long long X = (long long)p.B * p.nch * p.Hkv;  // chunks of the batch (with empty ones)
     const long long K_cta = X > c ? (X - c + C - 1) / C : 0;  // chunks c, c + C, ... of this CTA
 
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                            ~uintptr_t(1023));
     unsigned char *wbuf = smem + size_t(warp) * nbuf * CG::kBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + CG::bars_off(nbuf)) + warp * kChunkMaxBuf;
     ChunkSlot *slots = reinterpret_cast<ChunkSlot *>(smem + CG::slots_off(nbuf)) + warp * kChunkMaxBuf;
     int *s_next = reinterpret_cast<int *>(smem + CG::next_off(nbuf));
-
-    if (lane < nbuf) mbar_init(&bars[lane], 1);
-    if (threadIdx.x == 0) {
-        *s_next = 0;
-        prefetch_tensormap(&kmap);
-    }
-    fence_barrier_init();
-    __syncthreads();
-    // Nothing above touches global memory; the previous kernel in the stream (which
-    // may produce q, K or read this call's workspace) must be complete below.
-    pdl_wait();
-    // Only now may pass 2 start: it reads the call's inputs before its own
-    // dependency wait, and they are final once the kernel before this one is.
-    pdl_launch_dependents();
 
     // lane 0's cache of the last sequence's bounds
     int lb = -1, lL = 0;
@@ -257,20 +293,19 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 lb = b;
             }
             int len = min(kChunkRows, lL - ch * kChunkRows);
+            int rec = len > 0 ? 1 : 0;
             long long row = lstart + ch * kChunkRows;
             if (kPaged && len > 0) {
                 row = key_row<kPaged>(p, b, lstart, ch * kChunkRows);  // a chunk never straddles pages
                 if (row < 0) {  // bad page id (flagged): the chunk carries no mass
-                    for (int h = 0; h < G; ++h) {
-                        const size_t rec = (size_t(b) * p.Hq + kvh * G + h) * p.nch + ch;
-                        p.rec_m[rec] = -INFINITY;
-                        p.rec_z[rec] = 0.f;
-                    }
+                    for (int h = 0; h < G; ++h)
+                        store_record(p.rec + (size_t(b) * p.Hq + kvh * G + h) * p.nch + ch, -INFINITY, 0.f);
                     len = 0;
+                    rec = 1;
                 }
             }
             const int slot = n_issued % nbuf;
-            slots[slot] = ChunkSlot{lstart, b, ch, kvh, len};
+            slots[slot] = ChunkSlot{lstart, b, ch, kvh, len, rec};
             uint64_t *bar = &bars[slot];
             if (len > 0) {
                 unsigned char *dst = wbuf + size_t(slot) * CG::kBytes;
@@ -302,6 +337,20 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     }
 
     bool failed = false;
+    // Chunks of the current (sequence, KV head) whose records are stored but not yet
+    // published (warp-uniform).  Called once a chunk is finished: publishes them when
+    // the next chunk in flight belongs to another (sequence, KV head), or none is.
+    int pend = 0;
+    auto finished = [&](const ChunkSlot &cs) {
+        pend += cs.rec;
+        __syncwarp();  // lane 0's slot descriptors of the chunks claimed since
+        const bool last = n_done + 1 >= n_issued || slots[(n_done + 1) % nbuf].b != cs.b ||
+                          slots[(n_done + 1) % nbuf].kvh != cs.kvh;
+        if (pend > 0 && last) {
+            publish_chunks<G>(p, cs.b, cs.kvh, pend, lane);
+            pend = 0;
+        }
+    };
     while (n_done < n_issued) {
         const int slot = n_done % nbuf;
         if (!mbar_wait(&bars[slot], (n_done / nbuf) & 1)) {
@@ -313,8 +362,9 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
         const ChunkSlot cs = slots[slot];
         const int len = cs.len, b = cs.b, kvh = cs.kvh, ch = cs.ch;
         if (len <= 0) {  // nothing to read: pass the buffer on
-            ++n_done;
             if (more) claim();
+            finished(cs);
+            ++n_done;
             continue;
         }
         const unsigned char *base = wbuf + size_t(slot) * CG::kBytes;
@@ -363,17 +413,19 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 const int h = 2 * t + j;
                 if (h < G) {
                     const int hq = kvh * G + h;
-                    float *srow = p.stash + (size_t(b) * p.Hq + hq) * p.max_len + size_t(ch) * kChunkRows;
+                    float *srow = p.stash + ((size_t(b) * p.Hq + hq) * p.nch + ch) * kChunkRows;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         if (8 * k + g < len) srow[8 * k + g] = xv[j][k];
-                    if (g == 0) {
-                        const size_t rec = (size_t(b) * p.Hq + hq) * p.nch + ch;
-                        p.rec_m[rec] = m[j];
-                        p.rec_z[rec] = z[j];
-                    }
                 }
             }
+            if (g == 0) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (2 * t + j < G)
+                        store_record(p.rec + (size_t(b) * p.Hq + kvh * G + 2 * t + j) * p.nch + ch, m[j], z[j]);
+            }
+            finished(cs);
             ++n_done;
             continue;
         }
@@ -437,7 +489,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
 #pragma unroll
             for (int bt = 1; bt < kGH; ++bt) m = fmaxf(m, x[bt]);
             m = head_max<kGH>(m);
-            float *srow = p.stash + (size_t(b) * p.Hq + hq) * p.max_len + size_t(ch) * kChunkRows;
+            float *srow = p.stash + ((size_t(b) * p.Hq + hq) * p.nch + ch) * kChunkRows;
             float z = 0.f;
 #pragma unroll
             for (int bt = 0; bt < kGH; ++bt) {
@@ -449,12 +501,10 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
                 }
             }
             z = head_sum<kGH>(z);
-            if (lane < kGH) {  // g8 = 0, l8 = lane: head `lane` of the pass
-                const size_t rec = (size_t(b) * p.Hq + hq) * p.nch + ch;
-                p.rec_m[rec] = m;
-                p.rec_z[rec] = z;
-            }
+            if (lane < kGH)  // g8 = 0, l8 = lane: head `lane` of the pass
+                store_record(p.rec + (size_t(b) * p.Hq + hq) * p.nch + ch, m, z);
         }
+        finished(cs);
         ++n_done;
     }
 
@@ -470,6 +520,25 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
         }
         __syncwarp();
     }
+    return failed;  // warp-uniform
+}
+
+// Pass 1 alone (santa_prop_pass1 and the two-kernel prop path): one CTA of
+// kChunkWarps streaming warps per SM.  Launched with programmatic dependent launch:
+// a CTA sets up its barriers while the previous kernel drains and waits for it
+// before touching global memory.
+template <typename T, int D, int G, bool kPaged>
+__global__ void __launch_bounds__(kChunkWarps * 32, 1)
+    prop_stream_kernel(const __grid_constant__ CUtensorMap kmap, const Params p, int nbuf) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = align1024(smem_raw);
+    stream_setup<T, D, G>(kmap, smem, nbuf);
+    __syncthreads();
+    // Nothing above touches global memory; the previous kernel in the stream (which
+    // may produce q, K or read this call's workspace) must be complete below.
+    pdl_wait();
+    pdl_launch_dependents();
+    stream_chunks<T, D, G, kPaged>(kmap, p, nbuf, smem);
 }
 
 }  // namespace santa

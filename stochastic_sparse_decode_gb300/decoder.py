@@ -29,7 +29,8 @@ class Decoder:
     def workspace(self, mode: str) -> torch.Tensor:
         if mode not in self._ws:
             n = workspace_size(self.problem, MODES[mode])
-            self._ws[mode] = torch.empty(n, dtype=torch.uint8, device=self.device)
+            # zero-filled: a prop workspace must start zero (santa_workspace_init)
+            self._ws[mode] = torch.zeros(n, dtype=torch.uint8, device=self.device)
         return self._ws[mode]
 
     def debug_buffers(self, mode: str, sample_stride: int = 0):

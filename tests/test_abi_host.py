@@ -90,14 +90,15 @@ def _llama8b_problem(sd, **kw):
 
 
 def test_workspace_layout_matches_the_byte_model(sd):
-    """prop: 2 chunk-record arrays [B][Hq][ceil(max_len/32)] and the fp32 score
-    stash [B][Hq][max_len]; flash: 2 tile-record arrays [B][Hq][T] and the tile
-    estimates [B][Hq][T][d]; exact: the streaming warps' partial states; each
-    rounded up to 256 B."""
+    """prop: a 256-byte header, a published-chunk counter per (sequence, query head),
+    the chunk records [B][Hq][ceil(max_len/32)] as 64-bit words and the fp32 score
+    stash [B][Hq][32 ceil(max_len/32)]; flash: 2 tile-record
+    arrays [B][Hq][T] and the tile estimates [B][Hq][T][d]; exact: the streaming
+    warps' partial states; each rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _llama8b_problem(sd)
     T, nch = 32768 // 256, 32768 // 32
-    prop = 2 * r(1 * 32 * nch * 4) + r(32 * 32768 * 4)
+    prop = 256 + r(1 * 32 * 4) + r(1 * 32 * nch * 8) + r(32 * nch * 32 * 4)
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
     flash = 2 * r(1 * 32 * T * 4) + r(1 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_FLASH) == flash
@@ -109,16 +110,20 @@ def test_workspace_layout_matches_the_byte_model(sd):
     p = _llama8b_problem(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
     T, nch = 8, 32
     assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
-    assert sd.workspace_size(p, sd.MODE_PROP) == 2 * r(3 * 32 * nch * 4) + r(3 * 32 * 1000 * 4)
+    assert sd.workspace_size(p, sd.MODE_PROP) == 256 + r(3 * 32 * 4) + r(3 * 32 * nch * 8) + r(3 * 32 * nch * 32 * 4)
 
 
 def test_very_long_prop_contexts_are_unsupported_not_wrong(sd):
-    """Pass 2 keeps a CTA's share of the chunk records in shared memory: a max_len
-    past that is refused on the host (flash and exact still take it)."""
+    """The sampler sums a head's chunk masses as 64-bit fixed-point integers, exact
+    for up to 2^17 chunks (2^22 keys): a longer max_len is refused on the host,
+    before anything is enqueued (flash and exact still take it)."""
     p = _llama8b_problem(sd, max_len=32 * 1024 * 1024, total_tokens=32 * 1024 * 1024, tile=1024)
     n = ctypes.c_size_t(0)
+    assert sd.lib().santa_workspace_size(ctypes.byref(p), sd.MODE_PROP, ctypes.byref(n)) == sd.UNSUPPORTED
+    assert sd.lib().santa_workspace_size(ctypes.byref(p), sd.MODE_FLASH, ctypes.byref(n)) == sd.OK
+    assert _call_prop(sd, p, ws_bytes=1 << 40) == sd.UNSUPPORTED
+    p = _llama8b_problem(sd, max_len=1 << 22, total_tokens=1 << 22, tile=1024)
     assert sd.lib().santa_workspace_size(ctypes.byref(p), sd.MODE_PROP, ctypes.byref(n)) == sd.OK
-    assert _call_prop(sd, p) == sd.UNSUPPORTED
 
 
 @pytest.mark.parametrize("field,value,status", [

@@ -30,19 +30,30 @@ def built_library():
 
 
 def _both_ways(inp):
+    import stochastic_sparse_decode_gb300 as sd
+
     dec = decoder_for(inp)
     q, k, v, indptr, U = to_torch(inp)
     dbg1, b1 = dec.debug_buffers("prop")
     whole = dec("prop", q, k, v, indptr, U, debug=dbg1).clone()
     torch.cuda.synchronize()
     dbg2, b2 = dec.debug_buffers("prop")
-    dec.workspace("prop").fill_(0xA5)  # nothing of the whole call may carry over
+    ws = dec.workspace("prop")
+    ws.fill_(0xA5)  # nothing of the whole call may carry over
     dec.pass1(q, k, indptr, debug=dbg2)
     split = dec.pass2(v, indptr, U, debug=dbg2).clone()
-    again = dec.pass2(v, indptr, U).clone()
+    # pass 2 sets the records back to zero; with the header cleared as well (the
+    # fill above wrote it), the workspace serves the fused call again
+    sd.santa_workspace_init(dec.problem, sd.MODE_PROP, ws)
+    dbg3, b3 = dec.debug_buffers("prop")
+    again = dec("prop", q, k, v, indptr, U, debug=dbg3).clone()
+    # and a split pair right after a fused call needs no initialisation at all
+    dec.pass1(q, k, indptr)
+    split2 = dec.pass2(v, indptr, U).clone()
     torch.cuda.synchronize()
-    assert int(b1["error_flags"][0]) == 0 and int(b2["error_flags"][0]) == 0
-    return whole, split, again, b1, b2
+    for b in (b1, b2, b3):
+        assert int(b["error_flags"][0]) == 0
+    return whole, split, again, split2, b1, b2
 
 
 @pytest.mark.parametrize("name", ["ragged_edges", "llama8b_32k_b1"])
@@ -53,9 +64,10 @@ def test_pass1_then_pass2_matches_whole_call(name):
     else:
         w = get_workload(name)
     inp = generate(w)
-    whole, split, again, b1, b2 = _both_ways(inp)
+    whole, split, again, split2, b1, b2 = _both_ways(inp)
     assert torch.equal(whole, split)
     assert torch.equal(whole, again)
+    assert torch.equal(whole, split2)
     for key in ("sample_idx", "tile_count"):
         assert torch.equal(b1[key], b2[key]), key
     for key in ("tile_m", "tile_z"):
@@ -79,13 +91,14 @@ def test_pass2_on_a_workspace_pass1_did_not_fill_is_clamped_not_faulted():
     g = torch.Generator(device="cpu").manual_seed(7)
     vals = torch.tensor([float("nan"), float("inf"), -float("inf"), -1.0e30, 3.0e38, -7.0, 0.0, 1.0, 1e-30])
     ws[:] = vals[torch.randint(0, vals.numel(), (ws.numel(),), generator=g)].cuda()
-    # the chunk records (m, z): m = 0 everywhere and z alternating +20 / -19, so the
-    # masses' running sum goes up and down and the threshold counts cannot all be
+    # the chunk records, 64-bit words (m, z) after the 256-byte header and the
+    # [B][Hq] counters: m = 0 everywhere and z alternating +20 / -19, so the masses'
+    # running sum goes up and down and the threshold counts cannot all be
     # non-negative -- a clamp must fire
     nrec = w.batch * w.num_q_heads * (-(-max(w.lengths) // 32))
-    zoff = -(-nrec * 4 // 256) * 256 // 4
-    ws[:nrec] = 0.0
-    ws[zoff : zoff + nrec] = torch.where(torch.arange(nrec, device="cuda") % 2 == 0, 20.0, -19.0)
+    rec0 = (256 + -(-w.batch * w.num_q_heads * 4 // 256) * 256) // 8
+    z = torch.where(torch.arange(nrec, device="cuda") % 2 == 0, 20.0, -19.0).view(torch.int32).to(torch.int64)
+    ws.view(torch.int64)[rec0 : rec0 + nrec] = (z & 0xFFFFFFFF) << 32
     dbg, bufs = dec.debug_buffers("prop")
     out = dec.pass2(v, indptr, U, debug=dbg)
     flags = sd.santa_read_device_error(bufs["error_flags"])
@@ -95,3 +108,37 @@ def test_pass2_on_a_workspace_pass1_did_not_fill_is_clamped_not_faulted():
     for b, L in enumerate(inp.lengths):
         sel = idx[b][idx[b] >= 0]
         assert sel.size == 0 or (sel.min() >= 0 and sel.max() < max(int(L), 1))
+
+
+def test_a_sampler_wait_that_runs_out_flags_and_returns():
+    """The fused prop kernel's samplers wait, bounded, for their head's chunk records.
+    With santa_debug.wait_cycles = -2000 on the 32k layer each sampler waits ~1 us
+    for a publication that never comes (one chunk more than its head has) and gives
+    up: the call returns with SANTA_ERR_TIMEOUT raised and zeros in out, the context
+    stays usable, the workspace is marked poisoned (the next call writes zeros and
+    raises SANTA_ERR_WORKSPACE), and santa_workspace_init makes it whole again."""
+    import stochastic_sparse_decode_gb300 as sd
+
+    inp = generate(get_workload("llama8b_32k_b1"))
+    dec = decoder_for(inp)
+    q, k, v, indptr, U = to_torch(inp)
+    ref = decoder_for(inp)("prop", q, k, v, indptr, U).clone()  # a separate workspace
+
+    dbg, bufs = dec.debug_buffers("prop")
+    dbg.wait_cycles = -2000
+    out = dec("prop", q, k, v, indptr, U, debug=dbg)
+    flags = sd.santa_read_device_error(bufs["error_flags"])
+    assert flags & sd.ERR_TIMEOUT, f"flags {flags:#x}"
+    assert (flags >> 8) & 0xF == 3  # the location code of a sampler's wait
+    assert torch.isfinite(out).all()
+
+    dbg, bufs = dec.debug_buffers("prop")
+    out = dec("prop", q, k, v, indptr, U, debug=dbg)
+    assert sd.santa_read_device_error(bufs["error_flags"]) == sd.ERR_WORKSPACE
+    assert torch.count_nonzero(out) == 0
+
+    sd.santa_workspace_init(dec.problem, sd.MODE_PROP, dec.workspace("prop"))
+    dbg, bufs = dec.debug_buffers("prop")
+    out = dec("prop", q, k, v, indptr, U, debug=dbg)
+    assert sd.santa_read_device_error(bufs["error_flags"]) == 0
+    assert torch.equal(out, ref)

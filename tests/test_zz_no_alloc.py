@@ -58,6 +58,7 @@ def test_static_scratch_matches_the_workspace_entry_point(sd):
     for inp, (q, k, v, ind, U), got in zip(cases, dev, outs):
         p = _problem(sd, inp)
         ws = torch.empty(sd.workspace_size(p, sd.MODE_PROP), dtype=torch.uint8, device="cuda")
+        sd.santa_workspace_init(p, sd.MODE_PROP, ws)  # a fresh prop workspace starts zero-filled
         ref = torch.full_like(got, float("nan"))
         sd.santa_decode_prop(p, q, k, v, ind, U, ref, ws)
         torch.cuda.synchronize()
