@@ -28,7 +28,8 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 struct Layout {
     int Tmax = 0, nch = 0;
     size_t rec_m = 0, rec_z = 0, stash = 0, partial = 0, total = 0;
-    size_t cnt = 0, rec = 0, clear = 0;  // prop: counters, packed chunk records; bytes that start at zero
+    // prop: counters, packed chunk records, chunk argmax offsets; bytes that start at zero
+    size_t cnt = 0, rec = 0, amax = 0, clear = 0;
 };
 
 int check_problem(const santa_problem *p, int mode) {
@@ -56,9 +57,10 @@ int check_problem(const santa_problem *p, int mode) {
 //   prop:        a 256-byte header (its first word: nonzero = poisoned by a timeout),
 //                per (sequence, query head) the count of chunks pass 1 has published,
 //                the chunk records [B][Hq][nch] as 64-bit words (m, z), nch =
-//                ceil(max_len / 32), and the score stash [B][Hq][nch * 32]; the header
-//                counters and records must be zero before the first call (`clear` bytes
-//                from the start) and every call leaves them so;
+//                ceil(max_len / 32), the score stash [B][Hq][nch * 32], and per chunk
+//                the offset of its largest key [B][Hq][nch rounded up to 4] (bytes);
+//                the header, counters and records must be zero before the first call
+//                (`clear` bytes from the start) and every call leaves them so;
 //   flash:       tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d];
 //   exact:       per (sequence, streaming warp, head of the group) the partial state
 //                (M, Z) as rec_m [B][P][G][2] and O as [B][P][G][d], P the warps of
@@ -104,6 +106,8 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
         L->clear = off;
         L->stash = off;
         off += align256(n_rec * 32 * 4);
+        L->amax = off;
+        off += align256(size_t(p->batch) * p->num_q_heads * size_t((nch + 3) & ~3));
     } else {
         L->rec_m = off;
         off += align256(n_rec * 4);
@@ -275,6 +279,8 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
         prm.rec = reinterpret_cast<unsigned long long *>(ws + L.rec);
         prm.cnt = reinterpret_cast<unsigned int *>(ws + L.cnt);
         prm.stash = reinterpret_cast<float *>(ws + L.stash);
+        prm.amax = ws + L.amax;
+        prm.nch4 = (L.nch + 3) & ~3;
     } else {
         prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
         prm.rec_z = reinterpret_cast<float *>(ws + L.rec_z);

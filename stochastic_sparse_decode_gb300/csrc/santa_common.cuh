@@ -45,6 +45,9 @@ struct Params {
     unsigned long long *rec;  // prop: [B][Hq][nch] chunk records, (m_c, z_c) as one 64-bit
                               // word, z in the high half; 0 = not written (see store_record)
     unsigned int *cnt;        // prop: [B][Hq] chunks published to the head's sampler (publish_chunks)
+    unsigned char *amax;      // prop: [B][Hq][nch4] offset of each chunk's first key of largest logit
+    int nch4;                 // prop: nch rounded up to a multiple of 4 (the row stride of amax)
+    int full_cap;             // prop sampler: chunks of a head whose whole stash fits in its shared memory
     unsigned int *hdr;        // prop: workspace header word; nonzero = poisoned by a timeout
     long long wait_cycles;    // bound on a sampler's wait for its records (0: kWaitCycles)
     float *stash;          // prop: [B][Hq][nch * 32] exp(x - m_c), key i of sequence b at i
@@ -74,6 +77,11 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Ends an mbarrier's life, so that its shared memory may serve another purpose.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // Makes initialised barriers visible to the asynchronous (TMA) proxy.

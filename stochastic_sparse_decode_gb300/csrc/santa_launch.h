@@ -100,7 +100,8 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
 // Shared-memory needs, for validation on the host.
 size_t prop_pass1_smem(int dtype, int D, int G, int smem_optin);
 size_t prop_sampler_smem(int D, int sampler, int S);
-size_t prop_fused_smem(int dtype, int D, int G, int sampler, int S, int smem_optin, int *nbuf);
+size_t prop_fused_smem(int dtype, int D, int G, int sampler, int S, int nch, int smem_optin, int *nbuf,
+                       int *full_cap);
 size_t flash_tile_smem(int dtype, int D, int G, int tile);
 size_t exact_stream_smem(int dtype, int D, int G);
 int exact_stream_warps(int dtype, int D, int G);

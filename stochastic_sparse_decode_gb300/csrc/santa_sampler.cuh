@@ -300,6 +300,8 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
     float *scrf = reinterpret_cast<float *>(sm + L::kScrF);
     int *scri = reinterpret_cast<int *>(sm + L::kScrI);
     float *s_u = reinterpret_cast<float *>(sm + L::kU);
+    // the head's whole stash, when it fits (p.full_cap chunks; see below)
+    float *fst = s_u + ((sampler_slots(SAMPLER, p.S) + 3) & ~3);
 
     const size_t head = size_t(b) * p.Hq + hq;
     float *outp = p.out + head * D;
@@ -390,7 +392,7 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
                     timed_out = true;
                     break;
                 }
-                __nanosleep(missing > 1 ? 256 : 32);
+                __nanosleep(missing > 1 ? 128 : 32);
                 missing = 0;
 #pragma unroll
                 for (int i = 0; i < kSampReg; ++i)
@@ -411,7 +413,28 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
     // every load below (each thread fences after its own observation of the counter,
     // and the barrier below orders that before every thread's later loads).
     if constexpr (kWait) __threadfence();
-    if (samp_sync_or(timed_out)) {
+    // the largest-logit offsets of this thread's chunks (one word: four bytes), read
+    // while M is formed
+    const int ca0 = (nblk - 1) * kSampBlock + tid * kSampReg;
+    const unsigned amx = (nblk == 1 && ca0 < Nb && !kPaged)
+                             ? __ldcg(reinterpret_cast<const unsigned *>(p.amax + head * p.nch4 + ca0))
+                             : 0u;
+    // One barrier for M, a wait that timed out and a record pass 1 did not write.
+    mx = warp_max(mx);
+    const bool w_to = __any_sync(kFull, timed_out), w_em = __any_sync(kFull, empty_rec);
+    if (lane == 0) {
+        scrf[warp] = mx;
+        scri[warp] = (w_to ? 1 : 0) | (w_em ? 2 : 0);
+    }
+    samp_sync();
+    float M = scrf[0];
+    int wflags = scri[0];
+#pragma unroll
+    for (int w = 1; w < kSampWarps; ++w) {
+        M = fmaxf(M, scrf[w]);
+        wflags |= scri[w];
+    }
+    if (wflags & 1) {
         // SANTA_ERR_TIMEOUT with location code 3 (a sampler waiting for its head's
         // scores); the records of this call will never be reset: poison the workspace
         if (tid == 0) {
@@ -420,17 +443,48 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
         }
         *give_up = true;
         if (tid < D) outp[tid] = 0.f;
+        samp_sync();  // the scratch is reused by the next head
         return;
     }
-    if (tid == 0) p.cnt[head] = 0u;  // every publication of this call is in: reset for the next
-    // a record pass 1 did not write (no mass), or a count that disagrees: flagged
-    if (samp_sync_or(empty_rec) && tid == 0) raise_flag(p, SANTA_ERR_WORKSPACE);
-    mx = warp_max(mx);
-    if (lane == 0) scrf[warp] = mx;
-    samp_sync();
-    float M = scrf[0];
+    if (tid == 0) {
+        p.cnt[head] = 0u;  // every publication of this call is in: reset for the next
+        // a record pass 1 did not write (no mass), or a count that disagrees
+        if (wflags & 2) raise_flag(p, SANTA_ERR_WORKSPACE);
+    }
+    // The whole stash of a head of at most p.full_cap chunks, into shared memory while
+    // the reducer runs (the list rounds below then copy from it instead of loading).
+    const bool full = Nb <= p.full_cap;
+    if (full) {
+        const float *sseq0 = p.stash + head * size_t(p.nch) * kChunkRows;
+        for (int pi = tid; pi < Nb * 8; pi += kSampThreads) {
+            const int c = pi >> 3, q = pi & 7;
+            const int valid = min(max(Lb - c * kChunkRows - 4 * q, 0), 4);
+            cp_async_16(fst + c * kChunkRows + 4 * q, sseq0 + size_t(c) * kChunkRows + 4 * q, 4 * valid);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    // V rows that the gather will most likely read, fetched into L2 now so that the
+    // gather at the end finds them there: the largest key of every chunk that may
+    // hold a sample.  A chunk's share of the mass is at most 32 exp(m_c - M) (Z >= 1),
+    // below 1e-4 when m_c < M - 13, so those are skipped.  (Only when the head's
+    // records fit one block; a prefetch changes no result.)
+    if (nblk == 1 && !kPaged) {
+        const unsigned char *vb = static_cast<const unsigned char *>(p.v) +
+                                  ((size_t(start) * p.Hkv + hq / p.G) * D) * sizeof(T);
 #pragma unroll
-    for (int w = 1; w < kSampWarps; ++w) M = fmaxf(M, scrf[w]);
+        for (int i = 0; i < kSampReg; ++i) {
+            const int c = ca0 + i;
+            if (c < Nb && r[i] != 0ull && rec_m(r[i]) >= M - 13.f) {
+                const int key = c * kChunkRows + int((amx >> (8 * i)) & 31u);
+                if (key < Lb) {
+                    const unsigned char *row = vb + size_t(key) * p.Hkv * D * sizeof(T);
+#pragma unroll
+                    for (int off = 0; off < D * int(sizeof(T)); off += 128)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+                }
+            }
+        }
+    }
 
     // masses of the thread's chunks of block blk (records in r), inclusive local prefix
     auto masses = [&](int blk, u64 (&pl)[kSampReg]) {
@@ -567,6 +621,7 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
                     ++e;
                 }
             }
+            if (full) asm volatile("cp.async.wait_group 0;" ::: "memory");  // the barrier publishes it
             samp_sync();
             const int nl = min(kSampList, ntot - r0);
             // The round's samples are the thresholds [m_first, m_end) (each entry holds
@@ -593,16 +648,23 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
                     raise_flag(p, SANTA_ERR_WORKSPACE);
                     ne = ne < 1 ? 1 : 32;
                 }
-                // Their stashed scores, global to shared memory without a register on the
-                // way (cp.async, 16 bytes per copy: lane l copies pieces l, l + 32, ... of
-                // the ne x 8 pieces); keys past the sequence's end read as 0.
+                // Their stashed scores into the warp's rows: from the head's stash in shared
+                // memory, or else global to shared memory without a register on the way
+                // (cp.async); 16 bytes per copy, lane l copies pieces l, l + 32, ... of the
+                // ne x 8 pieces; keys past the sequence's end read as 0.
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int pi = lane + 32 * j, k = pi >> 3, q = pi & 7;
                     if (k < ne) {
                         const int ck = l_c[ea + k];
-                        const int valid = min(max(Lb - ck * kChunkRows - 4 * q, 0), 4);
-                        cp_async_16(wev + k * kEvStride + 4 * q, sseq + size_t(ck) * kChunkRows + 4 * q, 4 * valid);
+                        if (full) {
+                            *reinterpret_cast<float4 *>(wev + k * kEvStride + 4 * q) =
+                                *reinterpret_cast<const float4 *>(fst + ck * kChunkRows + 4 * q);
+                        } else {
+                            const int valid = min(max(Lb - ck * kChunkRows - 4 * q, 0), 4);
+                            cp_async_16(wev + k * kEvStride + 4 * q, sseq + size_t(ck) * kChunkRows + 4 * q,
+                                        4 * valid);
+                        }
                     }
                 }
                 if constexpr (kPaged) {
@@ -689,13 +751,23 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
 // ---- kernels
 
 // Shared memory of the fused kernel: the streaming layout, which the samplers then
-// reuse from its start (the chunk buffers are idle once the CTA's stream is done;
-// the mbarriers after them are left alone).
+// reuse from its start once the CTA's stream is done (its chunk buffers are idle and
+// its mbarriers invalidated), with room for a head's whole stash of full_cap chunks
+// after the sampler's own layout.
 template <typename T, int D, int G>
-__host__ __device__ inline size_t fused_smem_bytes(int nbuf, int nu) {
+__host__ __device__ inline size_t fused_smem_bytes(int nbuf, int nu, int full_cap) {
     const size_t s1 = ChunkGeom<T, D, G>::bytes(nbuf);
-    const size_t s2 = 1024 + SampSmem<D>::bytes(nu);
+    const size_t s2 = 1024 + SampSmem<D>::bytes((nu + 3) & ~3) + size_t(full_cap) * kChunkRows * 4;
     return s1 > s2 ? s1 : s2;
+}
+// The largest full_cap that keeps the fused kernel within `optin` bytes (at most the
+// chunks of the longest sequence).
+template <typename T, int D, int G>
+__host__ inline int fused_full_cap(int nbuf, int nu, int nch, size_t optin) {
+    const size_t base = 1024 + SampSmem<D>::bytes((nu + 3) & ~3);
+    if (base >= optin) return 0;
+    const size_t cap = (optin - base) / (kChunkRows * 4);
+    return int(cap < size_t(nch) ? cap : size_t(nch));
 }
 
 // Fused S2ANTA-prop: one persistent CTA of kChunkWarps warps per SM.  The warps first

@@ -395,11 +395,14 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
             for (int o = 4; o < 32; o <<= 1)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(kFull, m[j], o));
+            int am[2];  // the chunk's first key of largest logit, per head
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 z[j] = 0.f;
+                am[j] = kChunkRows;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 3; k >= 0; --k) {
+                    if (xv[j][k] == m[j]) am[j] = 8 * k + g;
                     xv[j][k] = __expf(xv[j][k] - m[j]);  // 0 for keys past the end
                     z[j] += xv[j][k];
                 }
@@ -407,7 +410,10 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1)
 #pragma unroll
-                for (int j = 0; j < 2; ++j) z[j] += __shfl_xor_sync(kFull, z[j], o);
+                for (int j = 0; j < 2; ++j) {
+                    z[j] += __shfl_xor_sync(kFull, z[j], o);
+                    am[j] = min(am[j], __shfl_xor_sync(kFull, am[j], o));
+                }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int h = 2 * t + j;
@@ -422,8 +428,11 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
             if (g == 0) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
-                    if (2 * t + j < G)
-                        store_record(p.rec + (size_t(b) * p.Hq + kvh * G + 2 * t + j) * p.nch + ch, m[j], z[j]);
+                    if (2 * t + j < G) {
+                        const size_t hq = size_t(b) * p.Hq + kvh * G + 2 * t + j;
+                        store_record(p.rec + hq * p.nch + ch, m[j], z[j]);
+                        p.amax[hq * p.nch4 + ch] = static_cast<unsigned char>(am[j]);
+                    }
             }
             finished(cs);
             ++n_done;
@@ -491,18 +500,24 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
             m = head_max<kGH>(m);
             float *srow = p.stash + ((size_t(b) * p.Hq + hq) * p.nch + ch) * kChunkRows;
             float z = 0.f;
+            int am = kChunkRows;  // the chunk's first key of largest logit
 #pragma unroll
             for (int bt = 0; bt < kGH; ++bt) {
                 const int key = bt * 4 * kKB + g8 * kKB + l8 / kGH;
                 if (key < len) {
+                    if (x[bt] == m) am = min(am, key);
                     const float e = __expf(x[bt] - m);
                     srow[key] = e;
                     z += e;
                 }
             }
             z = head_sum<kGH>(z);
-            if (lane < kGH)  // g8 = 0, l8 = lane: head `lane` of the pass
+#pragma unroll
+            for (int o = kGH; o < 32; o <<= 1) am = min(am, __shfl_xor_sync(kFull, am, o));
+            if (lane < kGH) {  // g8 = 0, l8 = lane: head `lane` of the pass
                 store_record(p.rec + (size_t(b) * p.Hq + hq) * p.nch + ch, m, z);
+                p.amax[(size_t(b) * p.Hq + hq) * p.nch4 + ch] = static_cast<unsigned char>(am);
+            }
         }
         finished(cs);
         ++n_done;
@@ -519,6 +534,8 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
                 }
         }
         __syncwarp();
+    } else if (lane < nbuf) {
+        mbar_inval(&bars[lane]);  // every copy has landed: the shared memory may be reused
     }
     return failed;  // warp-uniform
 }

@@ -91,14 +91,15 @@ def _llama8b_problem(sd, **kw):
 
 def test_workspace_layout_matches_the_byte_model(sd):
     """prop: a 256-byte header, a published-chunk counter per (sequence, query head),
-    the chunk records [B][Hq][ceil(max_len/32)] as 64-bit words and the fp32 score
-    stash [B][Hq][32 ceil(max_len/32)]; flash: 2 tile-record
+    the chunk records [B][Hq][ceil(max_len/32)] as 64-bit words, the fp32 score
+    stash [B][Hq][32 ceil(max_len/32)] and a largest-key byte per chunk (rows rounded
+    up to 4); flash: 2 tile-record
     arrays [B][Hq][T] and the tile estimates [B][Hq][T][d]; exact: the streaming
     warps' partial states; each rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _llama8b_problem(sd)
     T, nch = 32768 // 256, 32768 // 32
-    prop = 256 + r(1 * 32 * 4) + r(1 * 32 * nch * 8) + r(32 * nch * 32 * 4)
+    prop = 256 + r(1 * 32 * 4) + r(1 * 32 * nch * 8) + r(32 * nch * 32 * 4) + r(32 * nch)
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
     flash = 2 * r(1 * 32 * T * 4) + r(1 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_FLASH) == flash
@@ -110,7 +111,8 @@ def test_workspace_layout_matches_the_byte_model(sd):
     p = _llama8b_problem(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
     T, nch = 8, 32
     assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
-    assert sd.workspace_size(p, sd.MODE_PROP) == 256 + r(3 * 32 * 4) + r(3 * 32 * nch * 8) + r(3 * 32 * nch * 32 * 4)
+    assert sd.workspace_size(p, sd.MODE_PROP) == (256 + r(3 * 32 * 4) + r(3 * 32 * nch * 8) + r(3 * 32 * nch * 32 * 4)
+                                                  + r(3 * 32 * nch))
 
 
 def test_very_long_prop_contexts_are_unsupported_not_wrong(sd):
