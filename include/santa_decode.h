@@ -133,10 +133,10 @@ typedef struct {
     int sample_stride;       /* flash only: row length of sample_idx */
     unsigned int *error_flags;   /* device word; kernels OR SANTA_ERR_* bits into it */
     santa_event_t main_begin;    /* recorded on `stream` right before / after the */
-    santa_event_t main_end;      /* mode's dominant kernel (prop: the fused kernel, or
-                                    pass 1 when the passes run apart; flash tile;
+    santa_event_t main_end;      /* mode's dominant kernel (prop: pass 1, or the fused
+                                    kernel of santa_decode_prop_fused; flash tile;
                                     exact stream), for timing that kernel alone */
-    long long wait_cycles;       /* > 0: bound, in SM clock cycles, on a prop sampler's
+    long long wait_cycles;       /* > 0: bound, in SM clock cycles, on a fused prop sampler's
                                     wait for its head's scores (0: about 1 s); a wait
                                     that runs out raises SANTA_ERR_TIMEOUT.  < 0, a
                                     test of that path: each sampler waits |wait_cycles|
@@ -166,23 +166,45 @@ int santa_workspace_init(const santa_problem *p, int mode, void *workspace, size
 /*
  * S2ANTA-prop decode (paper notes, Key designs 1-2).
  * q, k, v, kv_indptr, U, out, workspace: device pointers as described above.
- * One persistent kernel on `stream`, one CTA per SM, all resident at once: its
- * streaming warps are pass 1 (scores, stash, one record per 32-key chunk) and
- * its sampler warps are pass 2, one head at a time (reducer over the
- * ceil(L_b / 32) chunk records, per-chunk systematic search, V gather,
- * deterministic combine), each head starting as soon as its records are all
- * written.  When the fused kernel's shared memory does not fit (stratified or
- * i.i.d. samplers with large S), the same two stages run as two kernels.
- * Workspace: a 256-byte header, the chunk records [B][Hq][ceil(max_len / 32)]
- * as 64-bit words, and the score stash [B][Hq][32 ceil(max_len / 32)] float32; zero-filled
- * once before first use (see santa_workspace_init).  Supported up to
- * max_len = 2^22 keys (longer is SANTA_UNSUPPORTED).  Returns a status; see the
- * conventions above.
+ * Two kernels on `stream`.  Pass 1 streams K, one CTA per SM: scores, the
+ * exponentiated-score stash and one record (m, z) per 32-key chunk.  Pass 2
+ * runs per head on a cluster of up to 8 CTAs: the reducer over the
+ * ceil(L_b / 32) chunk records (M, exact fixed-point CDF, per-chunk budgets),
+ * the per-chunk systematic search, the V gather, and a combine in a fixed
+ * order (the result is deterministic); it then sets the head's records back
+ * to zero.
+ * Workspace (santa_workspace_size bytes, 256-byte aligned regions): a 256-byte
+ * header, per head a published-chunk counter, the chunk records
+ * [B][Hq][ceil(max_len / 32)] as 64-bit words, per head a finished-split
+ * counter (set by pass 1), the score stash [B][Hq][32 ceil(max_len / 32)]
+ * float32, a byte per chunk and the fused kernel's per-split float32 sums;
+ * zero-filled once before first use (see santa_workspace_init).  Supported up
+ * to max_len = 2^22 keys (longer is SANTA_UNSUPPORTED).  Returns a status; see
+ * the conventions above.
  */
 int santa_decode_prop(const santa_problem *p, const void *q, const void *k, const void *v,
                       const long long *kv_indptr, const float *U, float *out,
                       void *workspace, size_t workspace_bytes, const santa_debug *dbg,
                       santa_stream_t stream);
+
+/*
+ * S2ANTA-prop in one persistent kernel: the same arguments, workspace and
+ * results (to rounding: the V sums are added in another order) as
+ * santa_decode_prop.  One CTA per SM, all resident at once: its warps first
+ * stream K (pass 1), then serve as pass 2, a head starting as soon as every
+ * chunk record of it is written (each CTA polls the records, with a bounded
+ * wait: SANTA_ERR_TIMEOUT, see santa_debug.wait_cycles).  When there are SMs
+ * to spare, a head's S thresholds are shared by up to 8 CTAs (its splits)
+ * whose sums the last one to finish adds in split order.  When the fused
+ * kernel's shared memory does not fit (stratified or i.i.d. samplers with
+ * large S) the two kernels of santa_decode_prop run instead.  On GB300 at 32k
+ * keys this form takes longer than the two kernels: the samplers' chain of
+ * dependent steps after the last record outlasts the second launch it saves.
+ */
+int santa_decode_prop_fused(const santa_problem *p, const void *q, const void *k, const void *v,
+                            const long long *kv_indptr, const float *U, float *out,
+                            void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                            santa_stream_t stream);
 
 /*
  * The two passes of santa_decode_prop as separate calls (same notes, Key design
@@ -197,8 +219,8 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
  *   santa_prop_pass2  reads the workspace as santa_prop_pass1 left it for the
  *                     same problem, V, kv_indptr and the offsets U; writes out
  *                     and dbg's tile and sample outputs, and sets the chunk
- *                     records back to zero (the workspace is then ready for any
- *                     prop call).  It follows santa_prop_pass1 on the same problem
+ *                     records and counters back to zero (the workspace is then
+ *                     ready for any prop call).  It follows santa_prop_pass1 on the same problem
  *                     and workspace in stream order.  On any other workspace the
  *                     records are whatever it holds: every index derived from them
  *                     is clamped into range (no out-of-bounds access), a record

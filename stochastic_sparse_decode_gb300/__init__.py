@@ -27,6 +27,7 @@ EXPORTS = (
     "santa_workspace_size",
     "santa_workspace_init",
     "santa_decode_prop",
+    "santa_decode_prop_fused",
     "santa_prop_pass1",
     "santa_prop_pass2",
     "santa_decode_prop_paged",
@@ -106,7 +107,8 @@ def lib() -> ctypes.CDLL:
         P, Dp = ctypes.POINTER(Problem), ctypes.POINTER(Debug)
         L.santa_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
         L.santa_workspace_init.argtypes = [P, ctypes.c_int, vp, sz, vp]
-        for name in ("santa_decode_prop", "santa_decode_prop_strat", "santa_decode_prop_iid", "santa_decode_flash"):
+        for name in ("santa_decode_prop", "santa_decode_prop_fused", "santa_decode_prop_strat", "santa_decode_prop_iid",
+                     "santa_decode_flash"):
             getattr(L, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_prop_pass1.argtypes = [P, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_prop_pass2.argtypes = [P, vp, vp, vp, vp, vp, sz, Dp, vp]
@@ -176,6 +178,12 @@ def _call(name, problem, args, workspace, debug, stream):
 def santa_decode_prop(problem, q, k, v, kv_indptr, U, out, workspace, debug=None, stream=None):
     """S2ANTA-prop decode: see santa_decode.h.  All tensors on the current CUDA device."""
     _call("santa_decode_prop", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(U), _ptr(out)],
+          workspace, debug, stream)
+
+
+def santa_decode_prop_fused(problem, q, k, v, kv_indptr, U, out, workspace, debug=None, stream=None):
+    """S2ANTA-prop decode in one persistent kernel: see santa_decode.h."""
+    _call("santa_decode_prop_fused", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(U), _ptr(out)],
           workspace, debug, stream)
 
 
@@ -251,14 +259,17 @@ def santa_read_device_error(error_flags, stream=None) -> int:
     return h.value
 
 
-MODES = {"prop": MODE_PROP, "strat": MODE_PROP, "iid": MODE_PROP, "flash": MODE_FLASH, "exact": MODE_EXACT}
+MODES = {"prop": MODE_PROP, "prop_fused": MODE_PROP, "strat": MODE_PROP, "iid": MODE_PROP, "flash": MODE_FLASH,
+         "exact": MODE_EXACT}
 
 
 def decode(mode: str, problem, q, k, v, kv_indptr, U, out, workspace, debug=None, stream=None):
-    """Dispatch by mode name ('prop', 'strat', 'iid', 'flash', 'exact'); U is the offsets
-    [B][Hq] for prop and flash, the uniforms [B][Hq][S] for strat and iid, ignored by exact."""
+    """Dispatch by mode name ('prop', 'prop_fused', 'strat', 'iid', 'flash', 'exact'); U is the
+    offsets [B][Hq] for prop and flash, the uniforms [B][Hq][S] for strat and iid, ignored by exact."""
     if mode == "prop":
         santa_decode_prop(problem, q, k, v, kv_indptr, U, out, workspace, debug, stream)
+    elif mode == "prop_fused":
+        santa_decode_prop_fused(problem, q, k, v, kv_indptr, U, out, workspace, debug, stream)
     elif mode == "strat":
         santa_decode_prop_strat(problem, q, k, v, kv_indptr, U, out, workspace, debug, stream)
     elif mode == "iid":

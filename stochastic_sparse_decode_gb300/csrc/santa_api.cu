@@ -28,8 +28,9 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 struct Layout {
     int Tmax = 0, nch = 0;
     size_t rec_m = 0, rec_z = 0, stash = 0, partial = 0, total = 0;
-    // prop: counters, packed chunk records, chunk argmax offsets; bytes that start at zero
-    size_t cnt = 0, rec = 0, amax = 0, clear = 0;
+    // prop: counters, packed chunk records, split counters, chunk argmax offsets, the
+    // splits' sums; bytes that start at zero
+    size_t cnt = 0, rec = 0, done = 0, amax = 0, part = 0, clear = 0;
 };
 
 int check_problem(const santa_problem *p, int mode) {
@@ -57,10 +58,12 @@ int check_problem(const santa_problem *p, int mode) {
 //   prop:        a 256-byte header (its first word: nonzero = poisoned by a timeout),
 //                per (sequence, query head) the count of chunks pass 1 has published,
 //                the chunk records [B][Hq][nch] as 64-bit words (m, z), nch =
-//                ceil(max_len / 32), the score stash [B][Hq][nch * 32], and per chunk
-//                the offset of its largest key [B][Hq][nch rounded up to 4] (bytes);
-//                the header, counters and records must be zero before the first call
-//                (`clear` bytes from the start) and every call leaves them so;
+//                ceil(max_len / 32), per head the count of its splits that are done
+//                (set to 0 by pass 1), the score stash [B][Hq][nch * 32], per chunk the offset of its
+//                largest key [B][Hq][nch rounded up to 4] (bytes), and the splits'
+//                sums [B][Hq][prop_split_bound][d]; the header, counters and records
+//                must be zero before the first call (`clear` bytes from the start) and
+//                every call leaves them so;
 //   flash:       tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d];
 //   exact:       per (sequence, streaming warp, head of the group) the partial state
 //                (M, Z) as rec_m [B][P][G][2] and O as [B][P][G][d], P the warps of
@@ -88,7 +91,7 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
     const double nrec = B * Hq * (prop ? nch : Tmax);
     double est = 2 * nrec * 4;
     if (prop)
-        est += nrec * 32 * 4;
+        est += nrec * 32 * 4 + B * Hq * (kPropMaxSplit * D * 4 + 4);
     else
         est += nrec * D * 4;
     if (est > 1e15) return SANTA_INVALID_ARG;
@@ -104,10 +107,15 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
         L->rec = off;
         off += align256(n_rec * 8);
         L->clear = off;
+        L->done = off;
+        off += align256(size_t(p->batch) * p->num_q_heads * 4);
         L->stash = off;
         off += align256(n_rec * 32 * 4);
         L->amax = off;
         off += align256(size_t(p->batch) * p->num_q_heads * size_t((nch + 3) & ~3));
+        L->part = off;
+        const long long heads = (long long)p->batch * p->num_q_heads;
+        off += align256(size_t(heads) * prop_split_bound(heads) * p->head_dim * 4);
     } else {
         L->rec_m = off;
         off += align256(n_rec * 4);
@@ -125,9 +133,12 @@ int smem_check(const santa_problem *p, int mode, int sampler, bool paged) {
     const int G = p->num_q_heads / p->num_kv_heads;
     size_t need = 0;
     if (mode == SANTA_MODE_PROP) {
-        (void)paged;  // the paged kernels use the same shared memory
         need = prop_pass1_smem(p->dtype, p->head_dim, G, int(kOptin));
-        const size_t s2 = prop_sampler_smem(p->head_dim, sampler, p->S);
+        int nsplit = 0, cps = 0;
+        if (prop_pass2_split((p->max_len + 31) / 32, p->tile, (long long)p->batch * p->num_q_heads, &nsplit, &cps) !=
+            cudaSuccess)
+            return SANTA_CUDA_ERROR;
+        const size_t s2 = prop_pass2_smem(p->head_dim, cps, sampler, p->S, paged);
         if (s2 > need) need = s2;
     } else if (mode == SANTA_MODE_FLASH) {
         need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
@@ -280,6 +291,9 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
         prm.cnt = reinterpret_cast<unsigned int *>(ws + L.cnt);
         prm.stash = reinterpret_cast<float *>(ws + L.stash);
         prm.amax = ws + L.amax;
+        prm.done = reinterpret_cast<unsigned int *>(ws + L.done);
+        prm.part = reinterpret_cast<float *>(ws + L.part);
+        prm.nsplit = 1;  // set by the launcher
         prm.nch4 = (L.nch + 3) & ~3;
     } else {
         prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
@@ -354,6 +368,13 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
                       const float *U, float *out, void *workspace, size_t workspace_bytes, const santa_debug *dbg,
                       santa_stream_t stream) {
     return run(SANTA_MODE_PROP, kSys, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream);
+}
+
+int santa_decode_prop_fused(const santa_problem *p, const void *q, const void *k, const void *v,
+                            const long long *kv_indptr, const float *U, float *out, void *workspace,
+                            size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
+    return run(SANTA_MODE_PROP, kSys, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream,
+               kPass1 | kPass2 | kFused);
 }
 
 int santa_prop_pass1(const santa_problem *p, const void *q, const void *k, const long long *kv_indptr,

@@ -20,6 +20,7 @@ constexpr int kWarpRows = 64;    // K/V rows per TMA chunk of one tile-kernel wa
 constexpr int kMergeThreads = 128;
 constexpr int kExactCtaBound = 160;  // exact: streaming CTAs at most (the workspace is sized for it)
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
+constexpr int kPropMaxSplit = 8;  // prop: CTAs sharing one head's thresholds, at most
 
 enum Mode { kProp = 0, kFlash = 1, kExact = 2 };
 // Thresholds of the prop sampler ("Stochastic Sparse Attention for Memory-Bound
@@ -47,7 +48,10 @@ struct Params {
     unsigned int *cnt;        // prop: [B][Hq] chunks published to the head's sampler (publish_chunks)
     unsigned char *amax;      // prop: [B][Hq][nch4] offset of each chunk's first key of largest logit
     int nch4;                 // prop: nch rounded up to a multiple of 4 (the row stride of amax)
-    int full_cap;             // prop sampler: chunks of a head whose whole stash fits in its shared memory
+    int nsplit;               // prop, fused kernel: CTAs per head, each taking an equal share of the S thresholds
+    int p2_split, p2_cps;     // prop pass 2 kernel: CTAs (one cluster) per head, chunks per CTA
+    float *part;              // prop: [B][Hq][nsplit][D] the splits' sums of V rows (nsplit > 1)
+    unsigned int *done;       // prop: [B][Hq] splits of the head that have stored their sum
     unsigned int *hdr;        // prop: workspace header word; nonzero = poisoned by a timeout
     long long wait_cycles;    // bound on a sampler's wait for its records (0: kWaitCycles)
     float *stash;          // prop: [B][Hq][nch * 32] exp(x - m_c), key i of sequence b at i
@@ -143,6 +147,23 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        : "memory");
+}
+// L2 policy for data that is read once: its lines are the first evicted, so that a
+// streamed K or V cache does not push out what the kernel reads again (records,
+// stash, code).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// tma_load_3d with an L2 cache policy (l2_evict_first).
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                                 int c2, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)), "l"(pol)
         : "memory");
 }
 

@@ -86,11 +86,27 @@ struct Timing {
     cudaEvent_t begin = nullptr, end = nullptr;
 };
 
+// CTAs that share one prop head's thresholds (its splits): the most that the
+// workspace has room for (kPropMaxSplit while the heads of a call number at most
+// 32, fewer beyond; a function of the shape alone, so that santa_workspace_size
+// needs no device) ...
+inline int prop_split_bound(long long heads) {
+    const long long n = heads > 0 ? 256 / heads : 1;
+    return n < 1 ? 1 : n > kPropMaxSplit ? kPropMaxSplit : int(n);
+}
+// ... and, within that, as many as give every SM of the device one CTA.
+inline int prop_nsplit(long long heads, int sms) {
+    const long long n = heads > 0 ? sms / heads : 1;
+    const int bound = prop_split_bound(heads);
+    return n < 1 ? 1 : n > bound ? bound : int(n);
+}
+
 // Mode launchers (one translation unit each).  `dtype` is SANTA_F32/SANTA_BF16.
 // kmap32: the K descriptor with boxes of 32 rows (the streaming pass-1 kernel).
-// stages: kPass1 | kPass2 (santa_decode_prop runs both: in one fused kernel when
-// its shared memory fits, else as two kernels in that order).
-enum { kPass1 = 1, kPass2 = 2 };
+// stages: kPass1 | kPass2 runs the streaming kernel and the pass-2 kernel in that
+// order; with kFused as well, the one fused kernel instead when its shared memory
+// fits (else the same two kernels).
+enum { kPass1 = 1, kPass2 = 2, kFused = 4 };
 cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm,
                         int stages);
 cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
@@ -99,9 +115,12 @@ cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, co
 
 // Shared-memory needs, for validation on the host.
 size_t prop_pass1_smem(int dtype, int D, int G, int smem_optin);
-size_t prop_sampler_smem(int D, int sampler, int S);
-size_t prop_fused_smem(int dtype, int D, int G, int sampler, int S, int nch, int smem_optin, int *nbuf,
-                       int *full_cap);
+// The pass-2 kernel's split of a head's nch chunks on this device: *nsplit CTAs
+// of *cps chunks each (whole tiles and whole warps), at most 8 per head, sized so
+// that the grid fills about two CTAs per SM.
+cudaError_t prop_pass2_split(int nch, int tile, long long heads, int *nsplit, int *cps);
+size_t prop_pass2_smem(int D, int cps, int sampler, int S, bool paged);
+size_t prop_fused_smem(int dtype, int D, int G, int sampler, int S, int smem_optin, int *nbuf);
 size_t flash_tile_smem(int dtype, int D, int G, int tile);
 size_t exact_stream_smem(int dtype, int D, int G);
 int exact_stream_warps(int dtype, int D, int G);

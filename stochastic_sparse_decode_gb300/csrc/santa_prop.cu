@@ -1,6 +1,8 @@
-// santa_prop.cu -- launch of S2ANTA-prop: the fused persistent kernel (pass 1 and
-// the samplers in one grid), or pass 1 and the sampler as two kernels.
+// santa_prop.cu -- launch of S2ANTA-prop: the streaming pass 1 and the cluster
+// pass 2 as two kernels, or the fused persistent kernel (pass 1 and the samplers
+// in one grid).
 #include "santa_launch.h"
+#include "santa_pass2.cuh"
 #include "santa_sampler.cuh"
 #include "santa_stream.cuh"
 
@@ -19,27 +21,22 @@ size_t prop_pass1_smem(int dtype, int d, int g, int smem_optin) {
     return bytes;
 }
 
-// The sampler alone: one CTA per (sequence, query head).
-size_t prop_sampler_smem(int d, int sampler, int S) {
+size_t prop_pass2_smem(int d, int cps, int sampler, int S, bool paged) {
     const int nu = sampler_slots(sampler, S);
-    return d == 128 ? SampSmem<128>::bytes(nu) : SampSmem<64>::bytes(nu);
+    return d == 128 ? Pass2Smem<uint16_t, 128>::bytes(cps, nu, paged) : Pass2Smem<uint16_t, 64>::bytes(cps, nu, paged);
 }
 
 // The fused kernel: the streaming layout with as many buffers per warp as fit,
-// which the samplers then reuse, with room for a head's whole stash of *full_cap
-// chunks; 0 if it does not fit.  *nbuf: the buffers per warp.
-size_t prop_fused_smem(int dtype, int d, int g, int sampler, int S, int nch, int smem_optin, int *nbuf,
-                       int *full_cap) {
+// which the samplers then reuse; 0 if it does not fit.  *nbuf: the buffers per warp.
+size_t prop_fused_smem(int dtype, int d, int g, int sampler, int S, int smem_optin, int *nbuf) {
     size_t bytes = 0;
     SANTA_DISPATCH(dtype, d, g, {
         using CG = ChunkGeom<T, D, G>;
         const int nb = CG::nbuf_for(size_t(smem_optin));
         const int nu = sampler_slots(sampler, S);
-        const int cap = nb ? fused_full_cap<T, D, G>(nb, nu, nch, size_t(smem_optin)) : 0;
-        const size_t need = nb ? fused_smem_bytes<T, D, G>(nb, nu, cap) : size_t(-1);
+        const size_t need = nb ? fused_smem_bytes<T, D, G>(nb, nu) : size_t(-1);
         bytes = need <= size_t(smem_optin) ? need : 0;
         if (nbuf) *nbuf = nb;
-        if (full_cap) *full_cap = cap;
         return cudaSuccess;
     });
     return bytes;
@@ -57,12 +54,12 @@ static void *fused_for(int sampler, bool paged) {
 }
 
 template <typename T, int D>
-static void *sampler_for(int sampler, bool paged) {
-    if (paged) return sampler == kSys ? reinterpret_cast<void *>(prop_sample_kernel<T, D, kSys, true>) : nullptr;
+static void *pass2_for(int sampler, bool paged) {
+    if (paged) return sampler == kSys ? reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys, true>) : nullptr;
     switch (sampler) {
-        case kSys: return reinterpret_cast<void *>(prop_sample_kernel<T, D, kSys, false>);
-        case kStrat: return reinterpret_cast<void *>(prop_sample_kernel<T, D, kStrat, false>);
-        case kIid: return reinterpret_cast<void *>(prop_sample_kernel<T, D, kIid, false>);
+        case kSys: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kSys, false>);
+        case kStrat: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kStrat, false>);
+        case kIid: return reinterpret_cast<void *>(prop_pass2_kernel<T, D, kIid, false>);
         default: return nullptr;
     }
 }
@@ -87,6 +84,26 @@ static cudaError_t device_limits(int *sms, int *smem_optin) {
     return cudaSuccess;
 }
 
+cudaError_t prop_pass2_split(int nch, int tile, long long heads, int *nsplit, int *cps) {
+    int sms = 0, optin = 0;
+    if (device_limits(&sms, &optin) != cudaSuccess) {  // no device (host-side validation): GB300's count
+        cudaGetLastError();
+        sms = 152;
+    }
+    const int unit = (tile / 32) > kPass2Warps ? tile / 32 : kPass2Warps;
+    int n = (nch + 127) / 128;
+    const long long fill = heads > 0 ? (2LL * sms + heads - 1) / heads : 1;  // splits for two CTAs per SM
+    if (n > fill) n = int(fill);
+    const int n_smem = (nch + 8191) / 8192;  // at most 8192 chunks of C, N and exp(m - M) per CTA
+    if (n < n_smem) n = n_smem;
+    n = n < 1 ? 1 : (n > kP2MaxSplit ? kP2MaxSplit : n);
+    int per = (nch + n - 1) / n;
+    per = (per + unit - 1) / unit * unit;
+    *nsplit = n;
+    *cps = per < unit ? unit : per;
+    return cudaSuccess;
+}
+
 cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm,
                         int stages) {
     int sms = 0, optin = 0;
@@ -100,12 +117,17 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
         const long long chunks = (long long)p.B * p.nch * p.Hkv;
         long long grid = sms >= p.Hkv ? (long long)(sms / p.Hkv) * p.Hkv : sms;
         if (grid > chunks) grid = chunks;
-        int nbf = 0, cap = 0;
-        size_t sf = prop_fused_smem(dtype, D, G, p.sampler, p.S, p.nch, optin, &nbf, &cap);
+        int nbf = 0;
+        size_t sf = prop_fused_smem(dtype, D, G, p.sampler, p.S, optin, &nbf);
+        Params ps = p;
+        ps.nsplit = prop_nsplit((long long)p.B * p.Hq, sms);  // the fused kernel's splits of a head
+        e0 = prop_pass2_split(p.nch, p.tile, (long long)p.B * p.Hq, &ps.p2_split, &ps.p2_cps);
+        if (e0 != cudaSuccess) return e0;
         cudaError_t e = cudaSuccess;
         auto kf = reinterpret_cast<void (*)(const CUtensorMap, const Params, int)>(fused_for<T, D, G>(p.sampler, paged));
         if (!kf) return cudaErrorInvalidValue;
-        if ((stages & kPass1) && (stages & kPass2) && sf) {
+        const bool fused = (stages & kFused) && (stages & kPass1) && (stages & kPass2);
+        if (fused && sf) {
             e = ensure_smem(kf, sf);
             if (e != cudaSuccess) return e;
             // the grid is sized so that every CTA is resident at once
@@ -114,7 +136,7 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
             if (e != cudaSuccess) return e;
             if ((long long)per_sm * sms < grid) sf = 0;  // it could not be: two kernels
         }
-        if ((stages & kPass1) && (stages & kPass2) && sf) {
+        if (fused && sf) {
             // The fused kernel.  A sampler waits for records that other CTAs write, so
             // every CTA must run at once: the grid is one CTA per SM, which the device
             // holds at once whenever this kernel has it to itself.  (A cooperative
@@ -124,15 +146,17 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
             // up with SANTA_ERR_TIMEOUT instead of hanging.  Launched early behind the
             // previous kernel (programmatic dependent launch), whose completion it
             // awaits before touching global memory.
-            Params pf = p;
-            pf.full_cap = cap;
             record_event(tm.begin, stream);
             e = launch_kernel(kf, dim3(unsigned(grid)), dim3(kChunkWarps * 32), sf, stream, true, 0, false, kmap32,
-                              pf, nbf);
+                              ps, nbf);
             if (e != cudaSuccess) return e;
             record_event(tm.end, stream);
             return cudaSuccess;
         }
+        // Pass 1 may launch early (programmatic dependent launch): behind a previous
+        // call's pass 2 it sets up while that kernel drains.  Pass 2 goes in plain
+        // stream order: launched early, its CTAs would only wait on SMs pass 1 is
+        // using (measured slower on GB300).
         if (stages & kPass1) {
             const int nbuf = CG::nbuf_for(size_t(optin));
             if (!nbuf) return cudaErrorNotSupported;
@@ -147,13 +171,13 @@ cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, c
             record_event(tm.end, stream);
         }
         if (!(stages & kPass2)) return cudaSuccess;
-        auto k2 = reinterpret_cast<void (*)(const Params)>(sampler_for<T, D>(p.sampler, paged));
+        auto k2 = reinterpret_cast<void (*)(const Params)>(pass2_for<T, D>(p.sampler, paged));
         if (!k2) return cudaErrorInvalidValue;
-        const size_t s2 = prop_sampler_smem(D, p.sampler, p.S);
+        const size_t s2 = Pass2Smem<T, D>::bytes(ps.p2_cps, sampler_slots(p.sampler, p.S), paged);
         e = ensure_smem(k2, s2);
         if (e != cudaSuccess) return e;
-        const long long items = (long long)p.B * p.Hq;
-        return launch_kernel(k2, dim3(unsigned(items)), dim3(kSampThreads), s2, stream, false, 0, false, p);
+        return launch_kernel(k2, dim3(unsigned(ps.p2_split), unsigned(p.Hq), unsigned(p.B)), dim3(kPass2Warps * 32),
+                             s2, stream, false, ps.p2_split, false, ps);
     });
 }
 

@@ -1,6 +1,6 @@
 // santa_sampler.cuh -- the S2ANTA-prop sampler of one (sequence, query head), and
-// the kernels that run it: the fused prop kernel (pass 1, then the samplers, in one
-// persistent grid) and the sampler alone (santa_prop_pass2).
+// the fused prop kernel that runs it (pass 1, then the samplers, in one persistent
+// grid).
 //
 // "Stochastic Sparse Attention for Memory-Bound Inference" (paper notes, Key
 // design 2): pass 1 leaves exponentiated scores and one partition record per
@@ -8,7 +8,9 @@
 // thresholds U + m/S (Key design 1) on the global CDF, a block's budget being the
 // number of thresholds in its CDF interval; pass 2 searches the stashed in-block
 // CDF for each threshold and averages the chosen V rows.  Here a block is a
-// 32-key chunk and one CTA of kSampWarps warps serves a whole head:
+// 32-key chunk, and nsplit CTAs of kSampWarps warps serve one head (its splits):
+// each runs steps 1-3 on all of the head's records, and then samples its own
+// share of the S thresholds:
 //
 //   1. records.  The head's chunk records, one 64-bit word (m_c, z_c) each, are
 //      read into registers, kSampReg consecutive chunks per thread (kSampBlock
@@ -29,8 +31,10 @@
 //      r_m = (t_m Z - C_{c-1}) / exp(m_c - M) on the chunk's own scale, the
 //      smallest key whose prefix exceeds r_m (clamped to the chunk's keys of
 //      positive score); the 32 lanes' V rows are then gathered together.
-//   4. out = (sum of the warps' sums, in warp order) / S.  Then the head's record
-//      words and count are set back to 0 for the next call.
+//   4. the split's sum = the sum of its warps' sums, in warp order; the split that
+//      finishes last adds the splits' sums in split order (a counter in the
+//      workspace, no wait): out = total / S.  It then sets the head's record words
+//      and published-chunk count back to 0 for the next call.
 //
 // The work of one head is a chain of dependent steps, so it is spread over all
 // warps of the CTA: a few chunks per thread in the reducer, a few list entries per
@@ -203,7 +207,7 @@ __device__ __forceinline__ void gather_queue(float (&acc)[D / 32], const T *vrow
     constexpr int kE = D / 32;
     constexpr int kBytes = kE * int(sizeof(T));  // 4, 8 or 16
     constexpr int kWords = kBytes / 4;
-    constexpr int kFlight = kBytes <= 8 ? 32 : 16;
+    constexpr int kFlight = kBytes <= 8 ? 16 : 16;
     for (int r0 = 0; r0 < n; r0 += kFlight) {
         uint32_t raw[kFlight][kWords];
 #pragma unroll
@@ -282,7 +286,7 @@ struct Thresholds {
 // record that reads 0 counts as a chunk without mass and raises SANTA_ERR_WORKSPACE.
 // *give_up: set after a wait timed out (the grid's later heads are not waited for).
 template <typename T, int D, int SAMPLER, bool kPaged, bool kWait>
-__device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, int tid, bool *give_up) {
+__device__ void sample_head(const Params &p, int b, int hq, int split, unsigned char *sm, int tid, bool *give_up) {
     using L = SampSmem<D>;
     using u64 = unsigned long long;
     constexpr int kE = D / 32;
@@ -300,8 +304,6 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
     float *scrf = reinterpret_cast<float *>(sm + L::kScrF);
     int *scri = reinterpret_cast<int *>(sm + L::kScrI);
     float *s_u = reinterpret_cast<float *>(sm + L::kU);
-    // the head's whole stash, when it fits (p.full_cap chunks; see below)
-    float *fst = s_u + ((sampler_slots(SAMPLER, p.S) + 3) & ~3);
 
     const size_t head = size_t(b) * p.Hq + hq;
     float *outp = p.out + head * D;
@@ -310,6 +312,8 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
     raw_bounds<kPaged>(p, b, &ind0, &ind1);
     const int Lb = checked_bounds(p, ind0, ind1, &start);
     const int Nb = (Lb + kChunkRows - 1) / kChunkRows;
+    // this split's thresholds: [s_lo, s_hi)
+    const int s_lo = int((long long)p.S * split / p.nsplit), s_hi = int((long long)p.S * (split + 1) / p.nsplit);
 
     // the thresholds' parameters (uniforms checked into range; the i.i.d. ones sorted)
     Thresholds<SAMPLER> th;
@@ -413,8 +417,8 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
     // every load below (each thread fences after its own observation of the counter,
     // and the barrier below orders that before every thread's later loads).
     if constexpr (kWait) __threadfence();
-    // the largest-logit offsets of this thread's chunks (one word: four bytes), read
-    // while M is formed
+    // the largest-logit offsets of this thread's chunks (one word: four bytes), for
+    // the prefetch below
     const int ca0 = (nblk - 1) * kSampBlock + tid * kSampReg;
     const unsigned amx = (nblk == 1 && ca0 < Nb && !kPaged)
                              ? __ldcg(reinterpret_cast<const unsigned *>(p.amax + head * p.nch4 + ca0))
@@ -446,35 +450,21 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
         samp_sync();  // the scratch is reused by the next head
         return;
     }
-    if (tid == 0) {
-        p.cnt[head] = 0u;  // every publication of this call is in: reset for the next
-        // a record pass 1 did not write (no mass), or a count that disagrees
-        if (wflags & 2) raise_flag(p, SANTA_ERR_WORKSPACE);
-    }
-    // The whole stash of a head of at most p.full_cap chunks, into shared memory while
-    // the reducer runs (the list rounds below then copy from it instead of loading).
-    const bool full = Nb <= p.full_cap;
-    if (full) {
-        const float *sseq0 = p.stash + head * size_t(p.nch) * kChunkRows;
-        for (int pi = tid; pi < Nb * 8; pi += kSampThreads) {
-            const int c = pi >> 3, q = pi & 7;
-            const int valid = min(max(Lb - c * kChunkRows - 4 * q, 0), 4);
-            cp_async_16(fst + c * kChunkRows + 4 * q, sseq0 + size_t(c) * kChunkRows + 4 * q, 4 * valid);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    }
-    // V rows that the gather will most likely read, fetched into L2 now so that the
-    // gather at the end finds them there: the largest key of every chunk that may
-    // hold a sample.  A chunk's share of the mass is at most 32 exp(m_c - M) (Z >= 1),
-    // below 1e-4 when m_c < M - 13, so those are skipped.  (Only when the head's
-    // records fit one block; a prefetch changes no result.)
-    if (nblk == 1 && !kPaged) {
+    // a record pass 1 did not write (no mass), or a count that disagrees
+    if (tid == 0 && (wflags & 2)) raise_flag(p, SANTA_ERR_WORKSPACE);
+    // V rows that the gather will most likely read, fetched into L2 while the list is
+    // formed: the largest key of every chunk that may hold a sample (each split of the
+    // head takes every nsplit-th chunk).  A chunk's share of the mass is at most
+    // 32 exp(m_c - M) (Z >= 1), below 1e-4 when m_c < M - 13, so those are skipped.
+    // (Only when the head's records fit one block; a prefetch changes no result.)
+    auto prefetch_v = [&]() {
+        if (nblk != 1 || kPaged) return;
         const unsigned char *vb = static_cast<const unsigned char *>(p.v) +
                                   ((size_t(start) * p.Hkv + hq / p.G) * D) * sizeof(T);
 #pragma unroll
         for (int i = 0; i < kSampReg; ++i) {
             const int c = ca0 + i;
-            if (c < Nb && r[i] != 0ull && rec_m(r[i]) >= M - 13.f) {
+            if (c < Nb && c % p.nsplit == split && r[i] != 0ull && rec_m(r[i]) >= M - 13.f) {
                 const int key = c * kChunkRows + int((amx >> (8 * i)) & 31u);
                 if (key < Lb) {
                     const unsigned char *row = vb + size_t(key) * p.Hkv * D * sizeof(T);
@@ -484,7 +474,7 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
                 }
             }
         }
-    }
+    };
 
     // masses of the thread's chunks of block blk (records in r), inclusive local prefix
     auto masses = [&](int blk, u64 (&pl)[kSampReg]) {
@@ -537,6 +527,7 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
         const u64 base = carry + samp_exclusive<u64>(masses(blk, pl), scr64, par, &bt);
         par ^= 1;
         if (nblk == 1) Z = bt;
+        prefetch_v();
         const float fZ = __ull2float_rn(Z);
         Zf = fZ / kMassScale;
         rZ = 1.0f / fZ;
@@ -569,7 +560,7 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
         // debug: m_t, Z_tile (on the m_t scale) and S_tile of the tiles of this block,
         // from the records (still in place) and the N values, staged in shared memory
         // (the list area is free until the list is built below)
-        if (dbg_tiles) {
+        if (dbg_tiles && split == 0) {
             int *sN = reinterpret_cast<int *>(sm + L::kEv);  // kSampBlock + 1 ints fit in the prefix buffers
 #pragma unroll
             for (int i = 0; i < kSampReg; ++i) sN[tid * kSampReg + i + 1] = nN[i];
@@ -595,11 +586,6 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
             }
             samp_sync();
         }
-        // this block's records have been read: set them back to 0 for the next call
-#pragma unroll
-        for (int i = 0; i < kSampReg; ++i)
-            if (c0 + i < Nb) recs[c0 + i] = 0ull;
-
         int ntot;
         const int off = samp_exclusive<int>(nsel, scri, par, &ntot);
         par ^= 1;
@@ -621,13 +607,13 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
                     ++e;
                 }
             }
-            if (full) asm volatile("cp.async.wait_group 0;" ::: "memory");  // the barrier publishes it
             samp_sync();
             const int nl = min(kSampList, ntot - r0);
-            // The round's samples are the thresholds [m_first, m_end) (each entry holds
-            // l_cnt of them from l_n0 on); every warp takes an even share, 32 at a time:
-            // lane = one threshold, its entry found by a binary search over l_n0.
-            const int m_first = l_n0[0], m_end = l_n0[nl - 1] + l_cnt[nl - 1];
+            // The round's samples are the thresholds [l_n0[0], l_n0[nl-1] + l_cnt[nl-1])
+            // (each entry holds l_cnt of them from l_n0 on); this split takes those in
+            // [s_lo, s_hi), every warp an even share of them, 32 at a time: lane = one
+            // threshold, its entry found by a binary search over l_n0.
+            const int m_first = max(l_n0[0], s_lo), m_end = min(l_n0[nl - 1] + l_cnt[nl - 1], s_hi);
             const int per = max(0, m_end - m_first + kSampWarps - 1) / kSampWarps;
             const int ws0 = m_first + warp * per, ws1 = min(ws0 + per, m_end);
             for (int g0 = ws0; g0 < ws1; g0 += 32) {
@@ -648,23 +634,16 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
                     raise_flag(p, SANTA_ERR_WORKSPACE);
                     ne = ne < 1 ? 1 : 32;
                 }
-                // Their stashed scores into the warp's rows: from the head's stash in shared
-                // memory, or else global to shared memory without a register on the way
-                // (cp.async); 16 bytes per copy, lane l copies pieces l, l + 32, ... of the
+                // Their stashed scores into the warp's rows, global to shared memory without
+                // a register on the way (cp.async); 16 bytes per copy, lane l copies pieces l, l + 32, ... of the
                 // ne x 8 pieces; keys past the sequence's end read as 0.
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int pi = lane + 32 * j, k = pi >> 3, q = pi & 7;
                     if (k < ne) {
                         const int ck = l_c[ea + k];
-                        if (full) {
-                            *reinterpret_cast<float4 *>(wev + k * kEvStride + 4 * q) =
-                                *reinterpret_cast<const float4 *>(fst + ck * kChunkRows + 4 * q);
-                        } else {
-                            const int valid = min(max(Lb - ck * kChunkRows - 4 * q, 0), 4);
-                            cp_async_16(wev + k * kEvStride + 4 * q, sseq + size_t(ck) * kChunkRows + 4 * q,
-                                        4 * valid);
-                        }
+                        const int valid = min(max(Lb - ck * kChunkRows - 4 * q, 0), 4);
+                        cp_async_16(wev + k * kEvStride + 4 * q, sseq + size_t(ck) * kChunkRows + 4 * q, 4 * valid);
                     }
                 }
                 if constexpr (kPaged) {
@@ -735,15 +714,50 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
         carry += bt;
     }
 
-    // ---- 4. the warps' sums in warp order; out = sum / S
+    // ---- 4. the warps' sums in warp order: the split's sum.  One split: out = sum / S.
+    // Several: each stores its sum, then counts itself in (after a fence) on the
+    // head's counter, which pass 1 set to 0; the split that counts last adds the
+    // splits' sums in split order, out = total / S.  The last one also sets the
+    // head's records and published-chunk count back to 0 for the next call (every
+    // split has read them by then).
 #pragma unroll
     for (int e = 0; e < kE; ++e) red[warp * D + lane * kE + e] = acc[e];
     samp_sync();
+    float sum = 0.f;
     if (tid < D) {
-        float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < kSampWarps; ++w) sum += red[w * D + tid];
-        outp[tid] = sum / float(p.S);
+    }
+    const int ns = p.nsplit;
+    bool last = true;
+    if (ns > 1) {
+        if (tid < D) p.part[(head * ns + split) * D + tid] = sum;
+        __threadfence();
+        samp_sync();
+        if (tid == 0) {
+            const unsigned before = atomicAdd(p.done + head, 1u);
+            // before >= ns: a counter pass 1 did not set (a workspace it did not fill);
+            // each split then writes its own sum, flagged
+            scri[2 * kSampWarps] = before < unsigned(ns) ? (before == unsigned(ns - 1) ? 1 : 0) : 2;
+            if (before >= unsigned(ns)) raise_flag(p, SANTA_ERR_WORKSPACE);
+        }
+        samp_sync();
+        const int verdict = scri[2 * kSampWarps];
+        last = verdict == 1;
+        if (verdict == 2 && tid < D) outp[tid] = sum / float(p.S);
+        if (last) {
+            __threadfence();  // acquire: the other splits' sums
+            if (tid < D) {
+                float tot = 0.f;
+                for (int k = 0; k < ns; ++k) tot += __ldcg(p.part + (head * ns + k) * D + tid);
+                sum = tot;
+            }
+        }
+    }
+    if (last) {
+        if (tid < D) outp[tid] = sum / float(p.S);
+        if (tid == 0) p.cnt[head] = 0u;
+        for (int c = tid; c < Nb; c += kSampThreads) recs[c] = 0ull;
     }
     samp_sync();  // red and the scratch are reused by the next head
 }
@@ -752,30 +766,20 @@ __device__ void sample_head(const Params &p, int b, int hq, unsigned char *sm, i
 
 // Shared memory of the fused kernel: the streaming layout, which the samplers then
 // reuse from its start once the CTA's stream is done (its chunk buffers are idle and
-// its mbarriers invalidated), with room for a head's whole stash of full_cap chunks
-// after the sampler's own layout.
+// its mbarriers invalidated).
 template <typename T, int D, int G>
-__host__ __device__ inline size_t fused_smem_bytes(int nbuf, int nu, int full_cap) {
+__host__ __device__ inline size_t fused_smem_bytes(int nbuf, int nu) {
     const size_t s1 = ChunkGeom<T, D, G>::bytes(nbuf);
-    const size_t s2 = 1024 + SampSmem<D>::bytes((nu + 3) & ~3) + size_t(full_cap) * kChunkRows * 4;
+    const size_t s2 = 1024 + SampSmem<D>::bytes((nu + 3) & ~3);
     return s1 > s2 ? s1 : s2;
-}
-// The largest full_cap that keeps the fused kernel within `optin` bytes (at most the
-// chunks of the longest sequence).
-template <typename T, int D, int G>
-__host__ inline int fused_full_cap(int nbuf, int nu, int nch, size_t optin) {
-    const size_t base = 1024 + SampSmem<D>::bytes((nu + 3) & ~3);
-    if (base >= optin) return 0;
-    const size_t cap = (optin - base) / (kChunkRows * 4);
-    return int(cap < size_t(nch) ? cap : size_t(nch));
 }
 
 // Fused S2ANTA-prop: one persistent CTA of kChunkWarps warps per SM.  The warps first
 // stream their CTA's share of K (pass 1, as prop_stream_kernel), then serve as the
-// sampler of the heads blockIdx.x, blockIdx.x + gridDim.x, ..., each as soon as its
-// records are complete.  Every CTA must be resident at once (cooperative launch): a
-// sampler waits on records that the streaming warps of other CTAs write, and no
-// streaming warp ever waits on a sampler.
+// sampler of the items blockIdx.x, blockIdx.x + gridDim.x, ... (item = head x
+// nsplit + split), each as soon as its head's records are complete.  Every CTA must
+// be resident at once: a sampler waits on records that the streaming warps of other
+// CTAs write (a bounded wait), and no streaming warp ever waits on a sampler.
 template <typename T, int D, int G, int SAMPLER, bool kPaged>
 __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     prop_fused_kernel(const __grid_constant__ CUtensorMap kmap, const Params p, int nbuf) {
@@ -794,25 +798,16 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     // a warp whose copy timed out may have left a copy in flight into the buffers:
     // then this CTA samples nothing (its heads read as zeros, the timeout is flagged)
     bool give_up = *s_failed != 0;
-    const long long items = (long long)p.B * p.Hq;
+    const long long items = (long long)p.B * p.Hq * p.nsplit;
     for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const long long head = it / p.nsplit;
         if (give_up) {
-            if (threadIdx.x < D) p.out[size_t(it) * D + threadIdx.x] = 0.f;
+            if (threadIdx.x < D) p.out[size_t(head) * D + threadIdx.x] = 0.f;
             continue;
         }
-        sample_head<T, D, SAMPLER, kPaged, true>(p, int(it / p.Hq), int(it % p.Hq), smem, int(threadIdx.x), &give_up);
+        sample_head<T, D, SAMPLER, kPaged, true>(p, int(head / p.Hq), int(head % p.Hq), int(it % p.nsplit), smem,
+                                                 int(threadIdx.x), &give_up);
     }
-}
-
-// The sampler alone (santa_prop_pass2 and the two-kernel prop path): one CTA of
-// kSampWarps warps per (sequence, query head), in stream order after pass 1.
-template <typename T, int D, int SAMPLER, bool kPaged>
-__global__ void __launch_bounds__(kSampThreads) prop_sample_kernel(const Params p) {
-    extern __shared__ __align__(16) unsigned char smem_s[];
-    bool give_up = false;
-    const long long it = blockIdx.x;
-    pdl_wait();
-    sample_head<T, D, SAMPLER, kPaged, false>(p, int(it / p.Hq), int(it % p.Hq), smem_s, int(threadIdx.x), &give_up);
 }
 
 }  // namespace santa

@@ -294,6 +294,10 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
             }
             int len = min(kChunkRows, lL - ch * kChunkRows);
             int rec = len > 0 ? 1 : 0;
+            // the group's finished-split counters start this call at 0 (published with
+            // the chunk, before any split of the head can count itself in)
+            if (ch == 0)
+                for (int h = 0; h < G; ++h) p.done[size_t(b) * p.Hq + kvh * G + h] = 0u;
             long long row = lstart + ch * kChunkRows;
             if (kPaged && len > 0) {
                 row = key_row<kPaged>(p, b, lstart, ch * kChunkRows);  // a chunk never straddles pages
@@ -313,7 +317,8 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
                 mbar_arrive_expect_tx(bar, CG::kBytes);
 #pragma unroll
                 for (int bx = 0; bx < Geo::kBoxes; ++bx)
-                    tma_load_3d(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, kvh, int(row));
+                    tma_load_3d_hint(dst + bx * kChunkBoxBytes, &kmap, bar, bx * Geo::kBoxElems, kvh, int(row),
+                                     l2_evict_first());
             } else {
                 mbar_arrive(bar);
             }

@@ -44,7 +44,7 @@ class Decoder:
             "tile_count": torch.full((B, Hq, T), -1, dtype=torch.int32, device=dev),
             "error_flags": torch.zeros(1, dtype=torch.int32, device=dev),
         }
-        if mode in ("prop", "strat", "iid"):
+        if mode in ("prop", "prop_fused", "strat", "iid"):
             bufs["sample_idx"] = torch.full((B, Hq, p.S), -1, dtype=torch.int32, device=dev)
         elif mode == "flash":
             bufs["sample_idx"] = torch.full((B, Hq, T, max(sample_stride, 1)), -1, dtype=torch.int32, device=dev)

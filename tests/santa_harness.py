@@ -92,7 +92,7 @@ def check(inp: Inputs, mode: str, res: dict, S: int | None = None, U_index: int 
     for b, h in (heads if heads is not None else pick_heads(inp, None)):
         q, K, V = head_slices(inp, b, h)
         what = f"{w.name}/{mode}/b{b}h{h}"
-        if mode == "prop":
+        if mode in ("prop", "prop_fused"):
             rep.merge(compare.check_prop_head(q, K, V, S, float(U[b, h]), w.tile, res["out"][b, h],
                                               res["sample_idx"][b, h], res["tile_count"][b, h],
                                               res["tile_m"][b, h], res["tile_z"][b, h], what=what))

@@ -34,7 +34,7 @@ def _report(name, rep):
 # ------------------------------------------------------------ tiny fp32 case
 
 
-@pytest.mark.parametrize("mode", ["prop", "flash", "exact"])
+@pytest.mark.parametrize("mode", ["prop", "prop_fused", "flash", "exact"])
 def test_tiny_fp32_all_offsets(mode):
     """batch 1, 4 q heads on 1 KV head, d=64, n_k=1024, tile 128, S=16: all 64 offsets."""
     inp = generate(get_workload("tiny_fp32"))
@@ -68,7 +68,7 @@ EDGE = [
 
 
 @pytest.mark.parametrize("case", range(len(EDGE)))
-@pytest.mark.parametrize("mode", ["prop", "flash", "exact"])
+@pytest.mark.parametrize("mode", ["prop", "prop_fused", "flash", "exact"])
 def test_edge_shapes(case, mode):
     """Empty, one-key, sub-tile and ragged-tail sequences; every GQA group size;
     tiles 32..1024; S from 1 to more than n_k; fp32 and bf16; d = 64 and 128."""
@@ -118,7 +118,8 @@ def llama8b_layer():
     return inp, to_torch(inp)
 
 
-@pytest.mark.parametrize("mode,S", [("prop", 128), ("prop", 256), ("flash", 2048), ("flash", 128), ("exact", 0)])
+@pytest.mark.parametrize("mode,S", [("prop", 128), ("prop", 256), ("prop_fused", 128), ("flash", 2048),
+                                    ("flash", 128), ("exact", 0)])
 def test_llama8b_32k_batch1(llama8b_layer, mode, S):
     """batch 1, 32 q / 8 KV heads, d=128, n_k=32768, tile 256: every head against the oracle."""
     inp, dev = llama8b_layer
@@ -138,11 +139,12 @@ def test_llama8b_32k_batch1(llama8b_layer, mode, S):
     assert np.array_equal(plain["out"], res["out"]), "debug outputs changed the result"
 
 
-def test_prop_is_deterministic(llama8b_layer):
+@pytest.mark.parametrize("mode", ["prop", "prop_fused"])
+def test_prop_is_deterministic(llama8b_layer, mode):
     """Two calls give bit-identical outputs (fixed-order combine, no float atomics)."""
     inp, dev = llama8b_layer
-    a = run(inp, "prop", dev_inputs=dev, debug=False)["out"]
-    b = run(inp, "prop", dev_inputs=dev, debug=False)["out"]
+    a = run(inp, mode, dev_inputs=dev, debug=False)["out"]
+    b = run(inp, mode, dev_inputs=dev, debug=False)["out"]
     assert np.array_equal(a, b)
 
 
@@ -155,7 +157,8 @@ def batch16():
     return inp, to_torch(inp)
 
 
-@pytest.mark.parametrize("mode,S", [("prop", 64), ("prop", 128), ("prop", 256), ("flash", 2048), ("exact", 0)])
+@pytest.mark.parametrize("mode,S", [("prop", 64), ("prop", 128), ("prop", 256), ("prop_fused", 128), ("flash", 2048),
+                                    ("exact", 0)])
 def test_llama8b_32k_batch16_sampled(batch16, mode, S):
     inp, dev = batch16
     U = draw_offsets(max(S, 1), (16, 32), np.random.default_rng(1000 + S))
@@ -164,7 +167,7 @@ def test_llama8b_32k_batch16_sampled(batch16, mode, S):
     _report(f"llama8b_32k_b16/{mode}/S{S}", check(inp, mode, res, S=S if S else None, U_values=U, heads=heads))
 
 
-@pytest.mark.parametrize("mode,S", [("prop", 128), ("flash", 2048), ("exact", 0)])
+@pytest.mark.parametrize("mode,S", [("prop", 128), ("prop_fused", 128), ("flash", 2048), ("exact", 0)])
 def test_ragged_batch64_sampled(mode, S):
     """64 sequences, n_k ~ UniformInt[4096, 32768], temperatures 0.5/1/2 per head."""
     w = get_workload("ragged_b64")

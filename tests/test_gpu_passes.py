@@ -43,16 +43,29 @@ def _both_ways(inp):
     dec.pass1(q, k, indptr, debug=dbg2)
     split = dec.pass2(v, indptr, U, debug=dbg2).clone()
     # pass 2 sets the records back to zero; with the header cleared as well (the
-    # fill above wrote it), the workspace serves the fused call again
+    # fill above wrote it), the workspace serves the fused kernel
     sd.santa_workspace_init(dec.problem, sd.MODE_PROP, ws)
     dbg3, b3 = dec.debug_buffers("prop")
-    again = dec("prop", q, k, v, indptr, U, debug=dbg3).clone()
-    # and a split pair right after a fused call needs no initialisation at all
+    fused_a = torch.empty_like(whole)
+    sd.santa_decode_prop_fused(dec.problem, q, k, v, indptr, U, fused_a, ws, dbg3)
+    # the fused kernel leaves the workspace as it found it: the two kernels, the split
+    # pair and the fused kernel again follow without any initialisation
+    dbg4, b4 = dec.debug_buffers("prop")
+    again = dec("prop", q, k, v, indptr, U, debug=dbg4).clone()
     dec.pass1(q, k, indptr)
     split2 = dec.pass2(v, indptr, U).clone()
+    fused_b = torch.empty_like(whole)
+    dbg5, b5 = dec.debug_buffers("prop")
+    sd.santa_decode_prop_fused(dec.problem, q, k, v, indptr, U, fused_b, ws, dbg5)
     torch.cuda.synchronize()
-    for b in (b1, b2, b3):
+    for b in (b1, b2, b3, b4, b5):
         assert int(b["error_flags"][0]) == 0
+    assert torch.equal(fused_a, fused_b)
+    # the fused kernel adds the same V rows in another order: equal to rounding
+    # wherever its samples are the two kernels' samples
+    same = (b3["sample_idx"] == b1["sample_idx"]).all(dim=-1)
+    assert same.float().mean() > 0.9
+    assert torch.allclose(fused_a[same], whole[same], rtol=0, atol=1e-5)
     return whole, split, again, split2, b1, b2
 
 
@@ -122,23 +135,23 @@ def test_a_sampler_wait_that_runs_out_flags_and_returns():
     inp = generate(get_workload("llama8b_32k_b1"))
     dec = decoder_for(inp)
     q, k, v, indptr, U = to_torch(inp)
-    ref = decoder_for(inp)("prop", q, k, v, indptr, U).clone()  # a separate workspace
+    ref = decoder_for(inp)("prop_fused", q, k, v, indptr, U).clone()  # a separate workspace
 
-    dbg, bufs = dec.debug_buffers("prop")
+    dbg, bufs = dec.debug_buffers("prop_fused")
     dbg.wait_cycles = -2000
-    out = dec("prop", q, k, v, indptr, U, debug=dbg)
+    out = dec("prop_fused", q, k, v, indptr, U, debug=dbg)
     flags = sd.santa_read_device_error(bufs["error_flags"])
     assert flags & sd.ERR_TIMEOUT, f"flags {flags:#x}"
     assert (flags >> 8) & 0xF == 3  # the location code of a sampler's wait
     assert torch.isfinite(out).all()
 
-    dbg, bufs = dec.debug_buffers("prop")
-    out = dec("prop", q, k, v, indptr, U, debug=dbg)
+    dbg, bufs = dec.debug_buffers("prop_fused")
+    out = dec("prop_fused", q, k, v, indptr, U, debug=dbg)
     assert sd.santa_read_device_error(bufs["error_flags"]) == sd.ERR_WORKSPACE
     assert torch.count_nonzero(out) == 0
 
-    sd.santa_workspace_init(dec.problem, sd.MODE_PROP, dec.workspace("prop"))
-    dbg, bufs = dec.debug_buffers("prop")
-    out = dec("prop", q, k, v, indptr, U, debug=dbg)
+    sd.santa_workspace_init(dec.problem, sd.MODE_PROP, dec.workspace("prop_fused"))
+    dbg, bufs = dec.debug_buffers("prop_fused")
+    out = dec("prop_fused", q, k, v, indptr, U, debug=dbg)
     assert sd.santa_read_device_error(bufs["error_flags"]) == 0
     assert torch.equal(out, ref)
