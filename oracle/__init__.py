@@ -17,6 +17,10 @@ Parity status of each function (pins live in ``tests/test_oracle_pins.py``):
 * flash (per-tile sampling + merge) .. pinned (exact integration over U,
   one-hot, uniform, S_loc = S/T closed form)
 * i.i.d. / stratified samplers ....... pinned (exact integration over u)
+* Bernoulli q K^T, per head and mean
+  group query ........................ pinned (exact enumeration of the draws:
+  E[c] = q, read probability 1 - prod (1-p)^draws; ternary entries; all p = 1
+  reduces to the exact query)
 """
 
 from __future__ import annotations
@@ -65,7 +69,9 @@ def _load():
         lib.oracle_prop_head.argtypes = [L, I, I, I, D, _dp, _dp, L, _dp, L, _dp, _lp, _ip, _dp, _dp]
         lib.oracle_sampled_head.argtypes = [I, L, I, I, _dp, _dp, _dp, L, _dp, L, _dp, _lp]
         lib.oracle_flash_head.argtypes = [L, I, I, I, D, _dp, _dp, L, _dp, L, _dp, _lp, _dp, _dp, _dp]
-        for f in ("oracle_exact_head", "oracle_prop_head", "oracle_sampled_head", "oracle_flash_head"):
+        lib.oracle_bernoulli_query.argtypes = [I, I, I, I, _dp, _dp, _dp, _ip]
+        for f in ("oracle_exact_head", "oracle_prop_head", "oracle_sampled_head", "oracle_flash_head",
+                  "oracle_bernoulli_query"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -153,6 +159,23 @@ def prop_head(q, K, V, S: int, U: float, tile: int, want_F: bool = True) -> Prop
     if rc != 0:
         raise MemoryError("oracle_prop_head")
     return PropHead(out, J if n > 0 else J[:0], counts[:T], mass[:T], F[:n] if want_F else None)
+
+
+def bernoulli_query(q, u, group_mean: bool) -> tuple[np.ndarray, np.ndarray]:
+    """Bernoulli q K^T for one KV group (oracle_bernoulli_query): q [G][d], u
+    [G or 1][draws][d] uniforms in [0, 1).  Returns the effective queries c [G][d]
+    (c_g . k estimates q_g . k) and the read mask [d] of the features selected."""
+    q, u = _f64(q), _f64(u)
+    G, d = q.shape
+    draws = u.shape[1]
+    assert u.shape == ((1 if group_mean else G), draws, d)
+    c = np.empty((G, d))
+    read = np.zeros(d, dtype=np.int32)
+    rc = _load().oracle_bernoulli_query(G, d, draws, int(bool(group_mean)), _ptr(q), _ptr(u), _ptr(c),
+                                         _ptr(read, _ip))
+    if rc < 0:
+        raise MemoryError("oracle_bernoulli_query")
+    return c, read.astype(bool)
 
 
 def sampled_head(mode: str, q, K, V, u) -> tuple[np.ndarray, np.ndarray]:

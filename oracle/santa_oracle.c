@@ -17,6 +17,12 @@
  *     Key design 3        S2ANTA-flash: every tile assumes it holds all the
  *                         mass and draws S/T samples; the merge rescales the
  *                         tile estimates by Z_tile / Z.
+ *     Key design 4        Bernoulli q K^T: the query scaled into [-1, 1] gives
+ *                         Bernoulli probabilities of a ternary {-1, 0, +1} query
+ *                         whose product with K estimates q K^T without bias, so
+ *                         only the features it selects are read from K.
+ *     Ablation table      mean group query: the GQA group's queries averaged
+ *                         before the draw, so the group shares one feature set.
  *   [DP]  "Double-P: Hierarchical Top-P Sparse Attention for Long-Context LLMs"
  *         (paper review), Stage 1, Eq. 3: logit x = q k^T / sqrt(d).
  *
@@ -29,6 +35,15 @@
  *   - samples are counted with multiplicity (the estimator of Key design 1);
  *   - flash: S_loc = ceil(S / T) samples per tile, all tiles share the offset
  *     U_t = U * S / S_loc in [0, 1/S_loc).
+ *   - Bernoulli q K^T: the scale into [-1, 1] is division by max_i |q_i|; a
+ *     ternary entry is drawn as sign(q_i) when a caller uniform u < |q_i| / max|q|
+ *     and 0 otherwise; `draws` independent draws are averaged; the estimate
+ *     replaces q in the logit (x = estimate of q k / sqrt(d)).  The mean group
+ *     query draws one selection per KV group from the mean of the group's
+ *     queries, p_i = |mean_i| / max|mean|, and head g weights a selected feature
+ *     by q_gi / p_i (the Horvitz-Thompson weight), so that every head's estimate
+ *     stays unbiased.  The draw decision (u < p) is taken in single precision,
+ *     the precision of the queries and uniforms, as the GPU takes it.
  *
  * Matrices are row-major; row i of K starts at K + i * ldk (likewise V).
  * Every function returns 0, or -1 if it could not allocate scratch memory.
@@ -377,4 +392,79 @@ int oracle_flash_head(long n, int d, int tile, int S, double U,
     free(ot);
     free(Jt);
     return S_loc;
+}
+
+/*
+ * Bernoulli q K^T ([SSA] Key design 4; mean group query: [SSA] ablation table)
+ * for one KV group of G query heads: the effective queries c_g such that
+ * c_g . k is the estimate of q_g . k for every key k.
+ *   q[G][d]              the group's queries (values of single precision)
+ *   u[ns][draws][d]      uniforms in [0, 1) (single precision values); ns = G
+ *                        (one draw set per head) or 1 (group_mean)
+ *   c[G][d]              out: the effective queries
+ *   read[d]              out: 1 if some draw of the group selected feature i
+ * Per head: p_gi = |q_gi| / max_j |q_gj|; draw b selects i when u[g][b][i] < p_gi,
+ * giving the ternary entry t = sign(q_gi), else 0; c_gi = max|q_g| * mean_b t.
+ * Group mean: qbar = (q_0 + ... + q_{G-1}) / G, p_i = |qbar_i| / max_j |qbar_j|;
+ * draw b selects i when u[0][b][i] < p_i; c_gi = (selections of i / draws) * q_gi / p_i.
+ * A query (or mean) of all zeros selects nothing: c = 0, and so does p_i = 0.
+ * Returns the number of features read.
+ */
+int oracle_bernoulli_query(int G, int d, int draws, int group_mean, const double *q, const double *u, double *c,
+                           int *read)
+{
+    int nread = 0;
+    for (int i = 0; i < d; ++i)
+        read[i] = 0;
+    if (!group_mean) {
+        for (int g = 0; g < G; ++g) {
+            const double *qg = q + (size_t)g * d;
+            float mx = 0.0f;
+            for (int i = 0; i < d; ++i) {
+                float a = fabsf((float)qg[i]);
+                if (a > mx)
+                    mx = a;
+            }
+            for (int i = 0; i < d; ++i) {
+                int hits = 0;
+                if (mx > 0.0f) {
+                    float p = fabsf((float)qg[i]) / mx;
+                    for (int b = 0; b < draws; ++b)
+                        hits += (float)u[((size_t)g * draws + b) * d + i] < p;
+                }
+                double sign = qg[i] > 0.0 ? 1.0 : (qg[i] < 0.0 ? -1.0 : 0.0);
+                c[(size_t)g * d + i] = (double)mx * sign * (double)hits / (double)draws;
+                if (hits > 0)
+                    read[i] = 1;
+            }
+        }
+    } else {
+        float *mean = malloc(sizeof(float) * (size_t)d);
+        if (!mean)
+            return -1;
+        float mx = 0.0f;
+        for (int i = 0; i < d; ++i) {
+            float s = 0.0f;
+            for (int g = 0; g < G; ++g)
+                s += (float)q[(size_t)g * d + i];
+            mean[i] = s / (float)G;
+            if (fabsf(mean[i]) > mx)
+                mx = fabsf(mean[i]);
+        }
+        for (int i = 0; i < d; ++i) {
+            int hits = 0;
+            float p = mx > 0.0f ? fabsf(mean[i]) / mx : 0.0f;
+            if (p > 0.0f)
+                for (int b = 0; b < draws; ++b)
+                    hits += (float)u[(size_t)b * d + i] < p;
+            for (int g = 0; g < G; ++g)
+                c[(size_t)g * d + i] = hits > 0 ? q[(size_t)g * d + i] / (double)p * (double)hits / (double)draws : 0.0;
+            if (hits > 0)
+                read[i] = 1;
+        }
+        free(mean);
+    }
+    for (int i = 0; i < d; ++i)
+        nread += read[i];
+    return nread;
 }

@@ -380,3 +380,132 @@ def test_page_figures_and_llama8b_v_row_fraction():
         assert 100.0 * len(rows) / w.length < bound
     # every head concentrates on its planted keys: far fewer than S distinct rows
     assert max(len(set(r.J.tolist())) for r in res.values()) < w.S
+
+
+# ------------------------------------------------------------------ Bernoulli q K^T
+# "Stochastic Sparse Attention for Memory-Bound Inference" (paper notes), Key
+# design 4: the ternary query drawn from q / max|q| estimates q K^T without bias;
+# ablation table: the mean group query shares one feature set across a GQA group.
+
+
+def _bernoulli_probs(q32: np.ndarray, group_mean: bool) -> np.ndarray:
+    """The draw probabilities in single precision: [G][d] per head, [1][d] for the
+    group mean (sum over heads in order, then / G)."""
+    if group_mean:
+        s = np.zeros(q32.shape[1], dtype=np.float32)
+        for g in range(q32.shape[0]):
+            s = (s + q32[g]).astype(np.float32)
+        mean = (s / np.float32(q32.shape[0])).astype(np.float32)
+        a = np.abs(mean)
+        return (a / a.max()).astype(np.float32)[None, :]
+    a = np.abs(q32)
+    return (a / a.max(axis=1, keepdims=True)).astype(np.float32)
+
+
+def _enumerate_draws(q32, draws, group_mean):
+    """Every outcome of the Bernoulli draws with its probability, realised through
+    uniforms (u = p/2 selects, u = (1+p)/2 does not); the oracle's c and read mask
+    for each.  Yields (probability, c, read)."""
+    import itertools
+
+    p = _bernoulli_probs(q32, group_mean)  # [ns][d]
+    ns, d = p.shape
+    n = ns * draws * d
+    pr = np.repeat(p[:, None, :], draws, axis=1).reshape(-1).astype(np.float64)
+    for bits in itertools.product((0, 1), repeat=n):
+        sel = np.array(bits, dtype=bool)
+        prob = float(np.prod(np.where(sel, pr, 1.0 - pr)))
+        if prob == 0.0:
+            continue
+        u = np.where(sel, pr / 2, (1.0 + pr) / 2).astype(np.float32).reshape(ns, draws, d)
+        c, read = oracle.bernoulli_query(q32.astype(np.float64), u.astype(np.float64), group_mean)
+        yield prob, c, read, p
+
+
+@pytest.mark.parametrize("group_mean", [False, True])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_bernoulli_query_is_unbiased_exactly(group_mean, seed):
+    """E[c_g] = q_g for every head, by exact enumeration of all draw outcomes
+    (d = 3, two draws; per head 2^12 outcomes, group mean 2^6), and the read
+    probability of feature i is 1 - prod (1 - p)^draws over the draw sets."""
+    rng = np.random.default_rng(seed)
+    G, d, draws = 2, 3, 2
+    q32 = rng.normal(size=(G, d)).astype(np.float32)
+    Ec = np.zeros((G, d))
+    Eread = np.zeros(d)
+    total = 0.0
+    p = None
+    for prob, c, read, p in _enumerate_draws(q32, draws, group_mean):
+        Ec += prob * c
+        Eread += prob * read
+        total += prob
+    assert abs(total - 1.0) < 1e-12
+    np.testing.assert_allclose(Ec, q32.astype(np.float64), rtol=1e-6, atol=1e-7)
+    p64 = p.astype(np.float64)
+    expect_read = 1.0 - np.prod((1.0 - p64) ** draws, axis=0)
+    np.testing.assert_allclose(Eread, expect_read, rtol=1e-12, atol=1e-12)
+
+
+def test_bernoulli_ternary_entries_and_monte_carlo():
+    """Per head one draw gives a ternary query: c / max|q| in {-1, 0, +1} with the
+    sign of q; over many draws the mean of c converges to q (5 sigma), and the
+    read fraction to its expectation."""
+    rng = np.random.default_rng(3)
+    G, d = 1, 64
+    q32 = rng.normal(size=(G, d)).astype(np.float32)
+    mx = float(np.abs(q32).max())
+    c, read = oracle.bernoulli_query(q32.astype(np.float64), rng.random((1, 1, d)), False)
+    t = c[0] / mx
+    assert set(np.unique(t)).issubset({-1.0, 0.0, 1.0})
+    assert np.all((t == 0) | (np.sign(t) == np.sign(q32[0])))
+    assert np.array_equal(read, t != 0)
+    n = 4000
+    acc = np.zeros(d)
+    sq = np.zeros(d)
+    nread = 0
+    for _ in range(n):
+        c, read = oracle.bernoulli_query(q32.astype(np.float64), rng.random((1, 1, d)), False)
+        acc += c[0]
+        sq += c[0] ** 2
+        nread += read.sum()
+    mean = acc / n
+    sd = np.sqrt(np.maximum(sq / n - mean ** 2, 1e-30) / n)
+    assert np.all(np.abs(mean - q32[0]) < 5 * sd + 1e-9)
+    p = np.abs(q32[0]).astype(np.float64) / mx
+    assert abs(nread / (n * d) - p.mean()) < 5 * np.sqrt(p.mean() * (1 - p.mean()) / (n * d)) + 1e-3
+
+
+@pytest.mark.parametrize("group_mean", [False, True])
+def test_bernoulli_with_all_probabilities_one_is_the_exact_query(group_mean):
+    """|q_i| all equal (and, for the group mean, equal heads): every p = 1, every
+    feature is read, c = q whatever the uniforms, and the prop head on c is the
+    prop head on q."""
+    rng = np.random.default_rng(5)
+    G, d, n = 2, 16, 300
+    row = np.where(rng.random(d) < 0.5, -0.75, 0.75).astype(np.float32)
+    q32 = np.stack([row, row if group_mean else -row])
+    ns = 1 if group_mean else G
+    c, read = oracle.bernoulli_query(q32.astype(np.float64), rng.random((ns, 3, d)), group_mean)
+    assert read.all()
+    np.testing.assert_array_equal(c, q32.astype(np.float64))
+    K = rng.normal(size=(n, d))
+    V = rng.normal(size=(n, d))
+    a = oracle.prop_head(c[0], K, V, 16, 0.01, 64)
+    b = oracle.prop_head(q32[0].astype(np.float64), K, V, 16, 0.01, 64)
+    np.testing.assert_array_equal(a.J, b.J)
+    np.testing.assert_array_equal(a.out, b.out)
+
+
+def test_mean_group_query_shares_one_feature_set():
+    """Mean group query: the read mask is the selection of the one shared draw
+    set, whatever the heads; per head, the union over heads (never smaller for
+    the same uniforms of head 0 when the heads are equal)."""
+    rng = np.random.default_rng(9)
+    G, d = 4, 32
+    q32 = rng.normal(size=(G, d)).astype(np.float32)
+    u = rng.random((1, 2, d))
+    c, read = oracle.bernoulli_query(q32.astype(np.float64), u, True)
+    p = _bernoulli_probs(q32, True)[0]
+    sel = (u.astype(np.float32) < p).any(axis=(0, 1))
+    assert np.array_equal(read, sel)
+    assert np.array_equal(c != 0, np.broadcast_to(sel, c.shape) & (q32 != 0))
