@@ -523,6 +523,9 @@ def run_ours(args, dist: Dist):
             dec("prop_fused", q, ks[i], vs[i], indptr, U, out=out)
         ms, _ = timed(n_x, min(args.warmup, 200), mode="prop_fused")
         extras["prop_fused_us_per_layer_step"] = round(ms * 1000.0 / n_x, 3)
+        # the Bernoulli ternary score stage on a feature-blocked K (four draws, as the
+        # pages' B = 4): the fraction of K features read and the call's time
+        extras.update(bernoulli_extras(dec, q, ks, vs, indptr, U, out, nrot, n_x, inp, bm, w))
         # the prop pipeline with the stratified and i.i.d. samplers, same S
         from synthetic.workloads import draw_uniforms
 
@@ -558,6 +561,65 @@ def run_ours(args, dist: Dist):
     if dist.rank == 0 and dist.world == 1:
         res["cpu_baseline"] = cpu_baseline(inp, args.mode, w.S, args.cpu_seconds)
         res["parity"] = oracle_parity(inp, args.mode, w.S, checked)
+    return res
+
+
+def bernoulli_extras(dec, q, ks, vs, indptr, U, out, nrot, nsteps, inp, bm, w) -> dict:
+    """santa_decode_prop_bernoulli on the timed workload, per head and with the mean
+    group query, four draws: the K-feature read fraction (the kept-feature counts
+    over the sequences' keys), the bytes it saves, and the call's time (graphs of
+    back-to-back calls over the rotating copies)."""
+    import torch
+
+    from synthetic.workloads import draw_uniforms
+
+    dev = q.device
+    kfbs = [dec.feature_blocked(ks[i]) for i in range(nrot)]
+    lengths = inp.lengths.astype(np.int64)
+    k_bytes = int(lengths.sum()) * w.num_kv_heads * w.head_dim * (2 if w.dtype == "bf16" else 4)
+    res = {}
+    for gm in (False, True):
+        tag = "bernoulli_group_mean" if gm else "bernoulli"
+        heads = w.num_kv_heads if gm else w.num_q_heads
+        bu = torch.from_numpy(draw_uniforms((w.batch, heads, 4, w.head_dim), np.random.default_rng(17))
+                              .astype(np.float32)).to(dev)
+        dbg, bufs = dec.debug_buffers("prop_bernoulli")
+        dec.prop_bernoulli(q, kfbs[0], vs[0], indptr, U, bu, 4, gm, out=out, debug=dbg)
+        torch.cuda.synchronize()
+        feat = bufs["features_read"].cpu().numpy().astype(np.int64)  # [B][Hkv]
+        frac = float((feat * lengths[:, None]).sum()) / max(1, int(lengths.sum()) * w.num_kv_heads * w.head_dim)
+        g = torch.cuda.CUDAGraph()
+        s_ = torch.cuda.Stream(device=dev)
+        s_.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_):
+            for i in range(nrot):
+                dec.prop_bernoulli(q, kfbs[i], vs[i], indptr, U, bu, 4, gm, out=out)
+        torch.cuda.current_stream().wait_stream(s_)
+        torch.cuda.synchronize()
+        n = min(nsteps, 200)
+        with torch.cuda.graph(g):
+            for i in range(n):
+                dec.prop_bernoulli(q, kfbs[i % nrot], vs[i % nrot], indptr, U, bu, 4, gm, out=out)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(5):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(int(2e6))
+            a_.record()
+            g.replay()
+            b_.record()
+            b_.synchronize()
+            reps.append(a_.elapsed_time(b_) * 1000.0 / n)
+        us = statistics.median(reps)
+        alg = bm["total"] - (1.0 - frac) * k_bytes  # the K features not kept are not read
+        res[f"{tag}_k_feature_read_fraction"] = round(frac, 4)
+        res[f"{tag}_k_bytes_saved_per_step"] = int(round((1.0 - frac) * k_bytes))
+        res[f"{tag}_us_per_layer_step"] = round(us, 3)
+        res[f"{tag}_hbm_gbs"] = round(alg / (us * 1e-6) / 1e9, 1)
+        del g
+    del kfbs
     return res
 
 

@@ -142,6 +142,9 @@ typedef struct {
                                     test of that path: each sampler waits |wait_cycles|
                                     for one chunk more than its head has, which never
                                     comes, and gives up */
+    int *features_read;          /* santa_decode_prop_bernoulli: [B][Hkv], the number of
+                                    features of d that some draw of the group kept
+                                    (the K features pass 1 read for that group) */
 } santa_debug;
 
 /*
@@ -204,6 +207,48 @@ int santa_decode_prop(const santa_problem *p, const void *q, const void *k, cons
 int santa_decode_prop_fused(const santa_problem *p, const void *q, const void *k, const void *v,
                             const long long *kv_indptr, const float *U, float *out,
                             void *workspace, size_t workspace_bytes, const santa_debug *dbg,
+                            santa_stream_t stream);
+
+/*
+ * S2ANTA-prop with the Bernoulli ternary score stage (paper notes, Key design 4;
+ * mean group query: the ablation table).  Instead of q . k, pass 1 computes an
+ * unbiased estimate of it and reads only the K features that the draws keep:
+ *   per head (group_mean = 0): p_i = |q_i| / max_j |q_j|; draw b keeps feature i
+ *     when bern_u[b][i] < p_i, as the ternary entry sign(q_i); the estimate is
+ *     max|q| * (mean over the draws of the ternary query) . k;
+ *   mean group query (group_mean = 1): one set of draws per KV group from the
+ *     mean of its G queries, p_i = |mean_i| / max_j |mean_j|; head g weights a
+ *     kept feature by q_gi / p_i (times the fraction of draws that kept it).
+ * The probabilities and the draw decisions are computed in single precision.  A
+ * group reads the union of the features any of its draws kept.
+ *   k_fb    the K cache in the feature-blocked layout of santa_k_feature_blocked
+ *           (16 keys of one feature per 32-byte sector for bf16), device
+ *   bern_u  float32 uniforms in [0, 1), device: [B][Hq][draws][d] per head, or
+ *           [B][Hkv][draws][d] for the mean group query
+ *   draws   1 .. 64 draws averaged per feature
+ * Every other argument, the workspace and the errors are those of
+ * santa_decode_prop (the same pass 2 runs on pass 1's records); dbg->
+ * features_read, when set, receives the kept-feature count of every group.
+ * Returns SANTA_INVALID_ARG for draws out of range or a missing bern_u.
+ */
+int santa_decode_prop_bernoulli(const santa_problem *p, const void *q, const void *k_fb, const void *v,
+                                const long long *kv_indptr, const float *U, const float *bern_u, int draws,
+                                int group_mean, float *out, void *workspace, size_t workspace_bytes,
+                                const santa_debug *dbg, santa_stream_t stream);
+
+/*
+ * The feature-blocked K layout of santa_decode_prop_bernoulli:
+ * K_fb[ceil(total_tokens / 16)][Hkv][d][16], element (row r, head h, feature f)
+ * at [r / 16][h][f][r % 16]; rows past total_tokens are zero.  *bytes receives
+ * its size; santa_k_feature_blocked writes it from the token-major cache k
+ * ([total_tokens][Hkv][d]) on `stream` (both device pointers, 16-byte aligned;
+ * the caller owns both).  A serving system would append keys in this layout
+ * directly; the conversion is for callers holding a token-major cache.
+ * Return SANTA_OK, SANTA_INVALID_ARG, SANTA_WORKSPACE_TOO_SMALL (k_fb_bytes too
+ * small) or SANTA_CUDA_ERROR.
+ */
+int santa_k_feature_blocked_size(const santa_problem *p, size_t *bytes);
+int santa_k_feature_blocked(const santa_problem *p, const void *k, void *k_fb, size_t k_fb_bytes,
                             santa_stream_t stream);
 
 /*

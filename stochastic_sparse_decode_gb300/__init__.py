@@ -28,6 +28,9 @@ EXPORTS = (
     "santa_workspace_init",
     "santa_decode_prop",
     "santa_decode_prop_fused",
+    "santa_decode_prop_bernoulli",
+    "santa_k_feature_blocked_size",
+    "santa_k_feature_blocked",
     "santa_prop_pass1",
     "santa_prop_pass2",
     "santa_decode_prop_paged",
@@ -76,6 +79,7 @@ class Debug(ctypes.Structure):
         ("main_begin", ctypes.c_void_p),
         ("main_end", ctypes.c_void_p),
         ("wait_cycles", ctypes.c_longlong),
+        ("features_read", ctypes.c_void_p),
     ]
 
 
@@ -111,6 +115,10 @@ def lib() -> ctypes.CDLL:
                      "santa_decode_flash"):
             getattr(L, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_prop_pass1.argtypes = [P, vp, vp, vp, vp, sz, Dp, vp]
+        L.santa_decode_prop_bernoulli.argtypes = [P, vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, sz,
+                                                  Dp, vp]
+        L.santa_k_feature_blocked_size.argtypes = [P, ctypes.POINTER(sz)]
+        L.santa_k_feature_blocked.argtypes = [P, vp, vp, sz, vp]
         L.santa_prop_pass2.argtypes = [P, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.santa_decode_prop_paged.argtypes = [P, ctypes.POINTER(Pages), vp, vp, vp, vp, vp, vp, sz, Dp, vp]
         L.exact_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, Dp, vp]
@@ -185,6 +193,32 @@ def santa_decode_prop_fused(problem, q, k, v, kv_indptr, U, out, workspace, debu
     """S2ANTA-prop decode in one persistent kernel: see santa_decode.h."""
     _call("santa_decode_prop_fused", problem, [_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(U), _ptr(out)],
           workspace, debug, stream)
+
+
+def santa_decode_prop_bernoulli(problem, q, k_fb, v, kv_indptr, U, bern_u, draws, group_mean, out, workspace,
+                                debug=None, stream=None):
+    """S2ANTA-prop with the Bernoulli ternary score stage on a feature-blocked K: see santa_decode.h."""
+    dbg = ctypes.byref(debug) if debug is not None else None
+    st = lib().santa_decode_prop_bernoulli(ctypes.byref(problem), _ptr(q), _ptr(k_fb), _ptr(v), _ptr(kv_indptr),
+                                           _ptr(U), _ptr(bern_u), int(draws), int(bool(group_mean)), _ptr(out),
+                                           _ptr(workspace), _nbytes(workspace), dbg, _stream(stream))
+    if st != OK:
+        raise SantaError(st, "santa_decode_prop_bernoulli")
+
+
+def k_feature_blocked_size(problem) -> int:
+    n = ctypes.c_size_t(0)
+    st = lib().santa_k_feature_blocked_size(ctypes.byref(problem), ctypes.byref(n))
+    if st != OK:
+        raise SantaError(st, "santa_k_feature_blocked_size")
+    return n.value
+
+
+def santa_k_feature_blocked(problem, k, k_fb, stream=None):
+    """The feature-blocked copy of the token-major K cache (santa_k_feature_blocked)."""
+    st = lib().santa_k_feature_blocked(ctypes.byref(problem), _ptr(k), _ptr(k_fb), _nbytes(k_fb), _stream(stream))
+    if st != OK:
+        raise SantaError(st, "santa_k_feature_blocked")
 
 
 def santa_prop_pass1(problem, q, k, kv_indptr, workspace, debug=None, stream=None):

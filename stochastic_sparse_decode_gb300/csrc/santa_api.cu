@@ -31,6 +31,8 @@ struct Layout {
     // prop: counters, packed chunk records, split counters, chunk argmax offsets, the
     // splits' sums; bytes that start at zero
     size_t cnt = 0, rec = 0, done = 0, amax = 0, part = 0, clear = 0;
+    // prop, Bernoulli score stage: effective queries, kept-feature lists, list lengths
+    size_t tq_c = 0, tq_list = 0, tq_cnt = 0;
 };
 
 int check_problem(const santa_problem *p, int mode) {
@@ -61,7 +63,9 @@ int check_problem(const santa_problem *p, int mode) {
 //                ceil(max_len / 32), per head the count of its splits that are done
 //                (set to 0 by pass 1), the score stash [B][Hq][nch * 32], per chunk the offset of its
 //                largest key [B][Hq][nch rounded up to 4] (bytes), and the splits'
-//                sums [B][Hq][prop_split_bound][d]; the header, counters and records
+//                sums [B][Hq][prop_split_bound][d], and for the Bernoulli score stage
+//                the effective queries [B][Hq][d] float, the kept features [B][Hkv][d]
+//                bytes and their counts [B][Hkv]; the header, counters and records
 //                must be zero before the first call (`clear` bytes from the start) and
 //                every call leaves them so;
 //   flash:       tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d];
@@ -116,6 +120,13 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
         L->part = off;
         const long long heads = (long long)p->batch * p->num_q_heads;
         off += align256(size_t(heads) * prop_split_bound(heads) * p->head_dim * 4);
+        const size_t groups = size_t(p->batch) * p->num_kv_heads;
+        L->tq_c = off;
+        off += align256(size_t(heads) * p->head_dim * 4);
+        L->tq_list = off;
+        off += align256(groups * p->head_dim);
+        L->tq_cnt = off;
+        off += align256(groups * 4);
     } else {
         L->rec_m = off;
         off += align256(n_rec * 4);
@@ -214,10 +225,15 @@ bool kv_map(CUtensorMap *map, const void *base, int dtype, int d, int hkv, long 
 // `stages` (prop only): which of the two passes to run; the other modes run whole.
 // Pass 1 alone needs q, k and kv_indptr; pass 2 alone needs v, kv_indptr, U and out.
 // `pages` (prop only): a paged cache; k and v are then the page pools and kv_indptr is unused.
+// `bern` (prop only): the Bernoulli score stage; k is then the feature-blocked K cache.
+struct Bern {
+    const float *u;
+    int draws, group_mean;
+};
 int run(int mode, int sampler, const santa_problem *p, const void *q, const void *k, const void *v,
         const long long *kv_indptr, const float *U, float *out, void *workspace, size_t workspace_bytes,
         const santa_debug *dbg, santa_stream_t stream_, int stages = kPass1 | kPass2,
-        const santa_pages *pages = nullptr) {
+        const santa_pages *pages = nullptr, const Bern *bern = nullptr) {
     int st = check_problem(p, mode);
     if (st != SANTA_OK) return st;
     if (sampler != kSys && p->S > kMaxSamplerS) return SANTA_UNSUPPORTED;
@@ -228,6 +244,9 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
             (long long)p->max_len > (long long)pages->max_pages * pages->page_size)
             return SANTA_INVALID_ARG;
     }
+    if (bern && (mode != SANTA_MODE_PROP || sampler != kSys || pages || stages != (kPass1 | kPass2) || !bern->u ||
+                 !aligned(bern->u, 4) || bern->draws < 1 || bern->draws > kMaxBernoulliDraws))
+        return SANTA_INVALID_ARG;
     if (p->batch == 0) return SANTA_OK;
     const bool p1 = stages & kPass1, p2 = stages & kPass2;
     if (pages && (!pages->page_table || !pages->kv_lens || !aligned(pages->page_table, 4) ||
@@ -315,7 +334,16 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
 
     CUtensorMap kmap, vmap;
     cudaError_t e;
-    if (mode == SANTA_MODE_PROP) {
+    if (bern) {
+        prm.bern_u = bern->u;
+        prm.draws = bern->draws;
+        prm.group_mean = bern->group_mean ? 1 : 0;
+        prm.tq_c = reinterpret_cast<float *>(ws + L.tq_c);
+        prm.tq_list = ws + L.tq_list;
+        prm.tq_cnt = reinterpret_cast<int *>(ws + L.tq_cnt);
+        prm.dbg_feat = dbg ? dbg->features_read : nullptr;
+        e = launch_prop_bernoulli(prm, p->dtype, stream, tm);
+    } else if (mode == SANTA_MODE_PROP) {
         if (p1 && !kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32))
             return SANTA_CUDA_ERROR;
         e = launch_prop(prm, p->dtype, kmap, stream, tm, stages);
@@ -375,6 +403,37 @@ int santa_decode_prop_fused(const santa_problem *p, const void *q, const void *k
                             size_t workspace_bytes, const santa_debug *dbg, santa_stream_t stream) {
     return run(SANTA_MODE_PROP, kSys, p, q, k, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream,
                kPass1 | kPass2 | kFused);
+}
+
+int santa_decode_prop_bernoulli(const santa_problem *p, const void *q, const void *k_fb, const void *v,
+                                const long long *kv_indptr, const float *U, const float *bern_u, int draws,
+                                int group_mean, float *out, void *workspace, size_t workspace_bytes,
+                                const santa_debug *dbg, santa_stream_t stream) {
+    const Bern bern{bern_u, draws, group_mean};
+    return run(SANTA_MODE_PROP, kSys, p, q, k_fb, v, kv_indptr, U, out, workspace, workspace_bytes, dbg, stream,
+               kPass1 | kPass2, nullptr, &bern);
+}
+
+int santa_k_feature_blocked_size(const santa_problem *p, size_t *bytes) {
+    if (!bytes) return SANTA_INVALID_ARG;
+    const int st = check_problem(p, SANTA_MODE_PROP);
+    if (st != SANTA_OK) return st;
+    const size_t esz = p->dtype == SANTA_BF16 ? 2 : 4;
+    *bytes = size_t((p->total_tokens + 15) / 16) * p->num_kv_heads * p->head_dim * 16 * esz;
+    return SANTA_OK;
+}
+
+int santa_k_feature_blocked(const santa_problem *p, const void *k, void *k_fb, size_t k_fb_bytes,
+                            santa_stream_t stream) {
+    size_t need = 0;
+    const int st = santa_k_feature_blocked_size(p, &need);
+    if (st != SANTA_OK) return st;
+    if (need == 0) return SANTA_OK;
+    if (!k || !k_fb || !aligned(k, 16) || !aligned(k_fb, 16)) return SANTA_INVALID_ARG;
+    if (k_fb_bytes < need) return SANTA_WORKSPACE_TOO_SMALL;
+    const cudaError_t e = launch_feature_block(p->dtype, k, k_fb, p->total_tokens, p->num_kv_heads, p->head_dim,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SANTA_OK : SANTA_CUDA_ERROR;
 }
 
 int santa_prop_pass1(const santa_problem *p, const void *q, const void *k, const long long *kv_indptr,

@@ -21,6 +21,7 @@ constexpr int kMergeThreads = 128;
 constexpr int kExactCtaBound = 160;  // exact: streaming CTAs at most (the workspace is sized for it)
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
 constexpr int kPropMaxSplit = 8;  // prop: CTAs sharing one head's thresholds, at most
+constexpr int kMaxBernoulliDraws = 64;  // Bernoulli score stage: draws per feature, at most
 
 enum Mode { kProp = 0, kFlash = 1, kExact = 2 };
 // Thresholds of the prop sampler ("Stochastic Sparse Attention for Memory-Bound
@@ -50,6 +51,14 @@ struct Params {
     int nch4;                 // prop: nch rounded up to a multiple of 4 (the row stride of amax)
     int nsplit;               // prop, fused kernel: CTAs per head, each taking an equal share of the S thresholds
     int p2_split, p2_cps;     // prop pass 2 kernel: CTAs (one cluster) per head, chunks per CTA
+    // prop, Bernoulli score stage: uniforms [B][Hq or Hkv][draws][D], per-group
+    // effective queries [B][Hq][D] and kept features [B][Hkv][D] in list order, and
+    // the list lengths [B][Hkv] (also copied to dbg_feat when given)
+    const float *bern_u;
+    int draws, group_mean;
+    float *tq_c;
+    unsigned char *tq_list;
+    int *tq_cnt, *dbg_feat;
     float *part;              // prop: [B][Hq][nsplit][D] the splits' sums of V rows (nsplit > 1)
     unsigned int *done;       // prop: [B][Hq] splits of the head that have stored their sum
     unsigned int *hdr;        // prop: workspace header word; nonzero = poisoned by a timeout

@@ -109,6 +109,11 @@ inline int prop_nsplit(long long heads, int sms) {
 enum { kPass1 = 1, kPass2 = 2, kFused = 4 };
 cudaError_t launch_prop(const Params &p, int dtype, const CUtensorMap &kmap32, cudaStream_t stream, const Timing &tm,
                         int stages);
+// S2ANTA-prop with the Bernoulli score stage: p.k is the feature-blocked K cache.
+cudaError_t launch_prop_bernoulli(const Params &p, int dtype, cudaStream_t stream, const Timing &tm);
+// Token-major K [rows][hkv][D] into the feature-blocked layout [ceil(rows/16)][hkv][D][16].
+cudaError_t launch_feature_block(int dtype, const void *k, void *kfb, long long rows, int hkv, int D,
+                                 cudaStream_t stream);
 cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
 cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          cudaStream_t stream, const Timing &tm);

@@ -13,8 +13,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (MODES, Debug, decode, make_pages, make_problem, santa_decode_prop_paged, santa_prop_pass1,
-               santa_prop_pass2, workspace_size)
+from . import (MODES, Debug, decode, k_feature_blocked_size, make_pages, make_problem, santa_decode_prop_bernoulli,
+               santa_decode_prop_paged, santa_k_feature_blocked, santa_prop_pass1, santa_prop_pass2, workspace_size)
 
 
 class Decoder:
@@ -44,8 +44,10 @@ class Decoder:
             "tile_count": torch.full((B, Hq, T), -1, dtype=torch.int32, device=dev),
             "error_flags": torch.zeros(1, dtype=torch.int32, device=dev),
         }
-        if mode in ("prop", "prop_fused", "strat", "iid"):
+        if mode in ("prop", "prop_fused", "strat", "iid", "prop_bernoulli"):
             bufs["sample_idx"] = torch.full((B, Hq, p.S), -1, dtype=torch.int32, device=dev)
+        if mode == "prop_bernoulli":
+            bufs["features_read"] = torch.full((B, p.num_kv_heads), -1, dtype=torch.int32, device=dev)
         elif mode == "flash":
             bufs["sample_idx"] = torch.full((B, Hq, T, max(sample_stride, 1)), -1, dtype=torch.int32, device=dev)
         dbg = Debug()
@@ -55,6 +57,8 @@ class Decoder:
         dbg.sample_idx = bufs["sample_idx"].data_ptr() if "sample_idx" in bufs else None
         dbg.sample_stride = int(sample_stride) if mode == "flash" else 0
         dbg.error_flags = bufs["error_flags"].data_ptr()
+        if "features_read" in bufs:
+            dbg.features_read = bufs["features_read"].data_ptr()
         return dbg, bufs
 
     def __call__(self, mode, q, k, v, kv_indptr, U=None, out=None, debug=None, stream=None) -> torch.Tensor:
@@ -85,4 +89,23 @@ class Decoder:
             out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=torch.float32, device=self.device)
         pages = make_pages(page_table, kv_lens, page_size, p.total_tokens // page_size)
         santa_decode_prop_paged(p, pages, q, k_pool, v_pool, U, out, self.workspace("prop"), debug, stream)
+        return out
+
+    def feature_blocked(self, k, stream=None) -> torch.Tensor:
+        """The feature-blocked copy of the token-major K cache k (santa_k_feature_blocked)."""
+        p = self.problem
+        esz = 2 if k.dtype in (torch.bfloat16, torch.int16, torch.uint16) else 4
+        n = k_feature_blocked_size(p)
+        kfb = torch.empty(n // esz, dtype=k.dtype, device=self.device)
+        santa_k_feature_blocked(p, k, kfb, stream)
+        return kfb
+
+    def prop_bernoulli(self, q, k_fb, v, kv_indptr, U, bern_u, draws, group_mean, out=None, debug=None,
+                       stream=None) -> torch.Tensor:
+        """S2ANTA-prop with the Bernoulli score stage (santa_decode_prop_bernoulli)."""
+        p = self.problem
+        if out is None:
+            out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=torch.float32, device=self.device)
+        santa_decode_prop_bernoulli(p, q, k_fb, v, kv_indptr, U, bern_u, draws, group_mean, out,
+                                    self.workspace("prop"), debug, stream)
         return out

@@ -93,15 +93,18 @@ def test_workspace_layout_matches_the_byte_model(sd):
     """prop: a 256-byte header, a published-chunk counter per (sequence, query head),
     the chunk records [B][Hq][ceil(max_len/32)] as 64-bit words, a finished-split
     counter per head, the fp32 score stash [B][Hq][32 ceil(max_len/32)], a
-    largest-key byte per chunk (rows rounded up to 4) and the splits' d-float sums,
-    min(8, 256 // (B Hq)) splits per head; flash: 2 tile-record
+    largest-key byte per chunk (rows rounded up to 4), the splits' d-float sums,
+    min(8, 256 // (B Hq)) splits per head, and the Bernoulli score stage's effective
+    queries [B][Hq][d] float, kept features [B][Hkv][d] bytes and their counts
+    [B][Hkv]; flash: 2 tile-record
     arrays [B][Hq][T] and the tile estimates [B][Hq][T][d]; exact: the streaming
     warps' partial states; each rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _llama8b_problem(sd)
     T, nch = 32768 // 256, 32768 // 32
+    tq = lambda B: r(B * 32 * 128 * 4) + r(B * 8 * 128) + r(B * 8 * 4)  # noqa: E731
     prop = (256 + r(1 * 32 * 4) + r(1 * 32 * nch * 8) + r(1 * 32 * 4) + r(32 * nch * 32 * 4) + r(32 * nch)
-            + r(32 * 8 * 128 * 4))
+            + r(32 * 8 * 128 * 4) + tq(1))
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
     flash = 2 * r(1 * 32 * T * 4) + r(1 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_FLASH) == flash
@@ -114,12 +117,13 @@ def test_workspace_layout_matches_the_byte_model(sd):
     T, nch = 8, 32
     assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_PROP) == (256 + r(3 * 32 * 4) + r(3 * 32 * nch * 8) + r(3 * 32 * 4)
-                                                  + r(3 * 32 * nch * 32 * 4) + r(3 * 32 * nch) + r(96 * 2 * 128 * 4))
+                                                  + r(3 * 32 * nch * 32 * 4) + r(3 * 32 * nch) + r(96 * 2 * 128 * 4)
+                                                  + tq(3))
     # a batch of 16 (512 heads): one split per head
     p = _llama8b_problem(sd, batch=16, max_len=1000, total_tokens=16000, tile=128)
     assert sd.workspace_size(p, sd.MODE_PROP) == (256 + r(16 * 32 * 4) + r(16 * 32 * nch * 8) + r(16 * 32 * 4)
                                                   + r(16 * 32 * nch * 32 * 4) + r(16 * 32 * nch)
-                                                  + r(16 * 32 * 1 * 128 * 4))
+                                                  + r(16 * 32 * 1 * 128 * 4) + tq(16))
 
 
 def test_very_long_prop_contexts_are_unsupported_not_wrong(sd):
