@@ -27,7 +27,8 @@
 
 namespace santa {
 
-constexpr int kFbWarps = 8;  // warps of a feature-blocked pass-1 CTA
+constexpr int kFbWarps = 8;   // warps of a feature-blocked pass-1 CTA
+constexpr int kFbBatch = 32;  // features whose loads a warp issues together
 
 // Effective queries and the kept-feature list of one (KV head, sequence).
 template <typename T, int G>
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(128) bernoulli_query_kernel(const Params p) {
 // with a stride of the grid's warp count; a warp stages its group's list and
 // effective queries in shared memory when its (sequence, KV head) changes.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kFbWarps * 32) fb_pass1_kernel(const Params p) {
+__global__ void __launch_bounds__(kFbWarps * 32, 3) fb_pass1_kernel(const Params p) {
     __shared__ int s_list[kFbWarps][D];
     __shared__ float s_c[kFbWarps][G][D];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -152,15 +153,29 @@ __global__ void __launch_bounds__(kFbWarps * 32) fb_pass1_kernel(const Params p)
         float x[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) x[g] = 0.f;
+        // kFbBatch features at a time: that many independent loads of the warp in flight
         int j = 0;
+        for (; j + kFbBatch <= nsel; j += kFbBatch) {
+            T kr[kFbBatch];
+#pragma unroll
+            for (int t = 0; t < kFbBatch; ++t) kr[t] = __ldg(kb + s_list[warp][j + t] * 16);
+#pragma unroll
+            for (int t = 0; t < kFbBatch; ++t) {
+                const float kv = to_float<T>(kr[t]);
+#pragma unroll
+                for (int g = 0; g < G; ++g) x[g] = fmaf(s_c[warp][g][j + t], kv, x[g]);
+            }
+        }
         for (; j + 8 <= nsel; j += 8) {
-            float kv[8];
+            T kr[8];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) kv[t] = to_float<T>(__ldg(kb + s_list[warp][j + t] * 16));
+            for (int t = 0; t < 8; ++t) kr[t] = __ldg(kb + s_list[warp][j + t] * 16);
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
+            for (int t = 0; t < 8; ++t) {
+                const float kv = to_float<T>(kr[t]);
 #pragma unroll
-                for (int g = 0; g < G; ++g) x[g] = fmaf(s_c[warp][g][j + t], kv[t], x[g]);
+                for (int g = 0; g < G; ++g) x[g] = fmaf(s_c[warp][g][j + t], kv, x[g]);
+            }
         }
         for (; j < nsel; ++j) {
             const float kv = to_float<T>(__ldg(kb + s_list[warp][j] * 16));
@@ -223,9 +238,9 @@ cudaError_t launch_prop_bernoulli(const Params &p, int dtype, cudaStream_t strea
         bernoulli_query_kernel<T, G><<<dim3(unsigned(p.Hkv), unsigned(p.B)), 128, 0, stream>>>(p);
         cudaError_t e1 = cudaGetLastError();
         if (e1 != cudaSuccess) return e1;
-        // four CTAs of 8 warps per SM: each warp keeps up to 8 of its key loads in flight
+        // three CTAs of 8 warps per SM, each warp with up to kFbBatch loads in flight
         const long long units = (long long)p.B * p.nch * p.Hkv;
-        long long grid = (long long)sms * 4;
+        long long grid = (long long)sms * 3;
         if (grid > (units + kFbWarps - 1) / kFbWarps) grid = (units + kFbWarps - 1) / kFbWarps;
         if (grid < 1) grid = 1;
         record_event(tm.begin, stream);
