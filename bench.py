@@ -58,7 +58,52 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
     ap.add_argument("--no-extras", action="store_true", help="skip the exact/flash comparison timings")
+    ap.add_argument("--profile", action="store_true",
+                    help="no benchmark: two rounds of one call of each path on the workload, for profiler "
+                         "captures (round 1 warms up; skip its " + str(PROFILE_ROUND_LAUNCHES) + " matched launches)")
     return ap.parse_args(argv)
+
+
+# The launches of one --profile round that the profiler filter
+# regex:"prop_stream|prop_pass2|fb_pass1|exact_stream|merge_kernel|tile_kernel|prop_fused" matches:
+# prop (stream, pass 2), Bernoulli with the mean group query (feature-blocked pass 1,
+# pass 2), exact (stream, merge), flash at S = 2048 (tiles, merge), the fused kernel.
+PROFILE_ROUND_LAUNCHES = 9
+
+
+def run_profile(args) -> dict:
+    """Two rounds of one call of each path (prop, Bernoulli mean group query, exact,
+    flash at S = 2048, fused prop) on the workload: a short, fixed launch sequence
+    for profiler captures of every kernel on the same inputs."""
+    import torch
+
+    from stochastic_sparse_decode_gb300.build import build
+    from stochastic_sparse_decode_gb300.decoder import Decoder
+    from synthetic import generate, get_workload, max_length, to_torch
+    from synthetic.workloads import draw_offsets, draw_uniforms
+
+    build()
+    dev = torch.device("cuda", 0)
+    w = get_workload(args.workload)
+    inp = generate(w)
+    q, k, v, indptr, U = to_torch(inp, dev)
+    dec = Decoder(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, inp.total_tokens, max_length(w), w.tile,
+                  w.S, w.dtype, device=dev)
+    decf = Decoder(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, inp.total_tokens, max_length(w), w.tile,
+                   2048, w.dtype, device=dev)
+    Uf = torch.from_numpy(draw_offsets(2048, (w.batch, w.num_q_heads), np.random.default_rng(7))).to(dev)
+    bu = torch.from_numpy(draw_uniforms((w.batch, w.num_kv_heads, 4, w.head_dim), np.random.default_rng(17))
+                          .astype(np.float32)).to(dev)
+    kfb = dec.feature_blocked(k)
+    out = torch.empty((w.batch, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        dec("prop", q, k, v, indptr, U, out=out)
+        dec.prop_bernoulli(q, kfb, v, indptr, U, bu, 4, True, out=out)
+        dec("exact", q, k, v, indptr, U, out=out)
+        decf("flash", q, k, v, indptr, Uf, out=out)
+        dec("prop_fused", q, k, v, indptr, U, out=out)
+        torch.cuda.synchronize()
+    return {"profile": w.name, "launches_per_round": PROFILE_ROUND_LAUNCHES}
 
 
 class Dist:
@@ -790,6 +835,9 @@ def main(argv=None):
         if int(os.environ.get("RANK", "0")) != 0:
             return 0
         print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if args.profile:
+        print(json.dumps(run_profile(args)), flush=True)
         return 0
     dist = Dist()
     if args.gpus != dist.world and dist.world > 1:

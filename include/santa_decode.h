@@ -222,7 +222,7 @@ int santa_decode_prop_fused(const santa_problem *p, const void *q, const void *k
  * The probabilities and the draw decisions are computed in single precision.  A
  * group reads the union of the features any of its draws kept.
  *   k_fb    the K cache in the feature-blocked layout of santa_k_feature_blocked
- *           (16 keys of one feature per 32-byte sector for bf16), device
+ *           (64 keys of one feature per 128-byte line for bf16), device
  *   bern_u  float32 uniforms in [0, 1), device: [B][Hq][draws][d] per head, or
  *           [B][Hkv][draws][d] for the mean group query
  *   draws   1 .. 64 draws averaged per feature
@@ -238,8 +238,8 @@ int santa_decode_prop_bernoulli(const santa_problem *p, const void *q, const voi
 
 /*
  * The feature-blocked K layout of santa_decode_prop_bernoulli:
- * K_fb[ceil(total_tokens / 16)][Hkv][d][16], element (row r, head h, feature f)
- * at [r / 16][h][f][r % 16]; rows past total_tokens are zero.  *bytes receives
+ * K_fb[ceil(total_tokens / 64)][Hkv][d][64], element (row r, head h, feature f)
+ * at [r / 64][h][f][r % 64]; rows past total_tokens are zero.  *bytes receives
  * its size; santa_k_feature_blocked writes it from the token-major cache k
  * ([total_tokens][Hkv][d]) on `stream` (both device pointers, 16-byte aligned;
  * the caller owns both).  A serving system would append keys in this layout

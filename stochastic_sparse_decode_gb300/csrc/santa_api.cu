@@ -419,7 +419,7 @@ int santa_k_feature_blocked_size(const santa_problem *p, size_t *bytes) {
     const int st = check_problem(p, SANTA_MODE_PROP);
     if (st != SANTA_OK) return st;
     const size_t esz = p->dtype == SANTA_BF16 ? 2 : 4;
-    *bytes = size_t((p->total_tokens + 15) / 16) * p->num_kv_heads * p->head_dim * 16 * esz;
+    *bytes = size_t((p->total_tokens + 63) / 64) * p->num_kv_heads * p->head_dim * 64 * esz;
     return SANTA_OK;
 }
 

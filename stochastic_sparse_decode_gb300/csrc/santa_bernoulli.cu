@@ -15,12 +15,14 @@
 //      queries and uniforms are), the draws (u < p), the effective queries
 //      c_g = estimate weights, and the group's list of features kept by any draw,
 //      compacted in feature order, with c stored in list order.
-//   2. fb_pass1_kernel, pass 1 on a feature-blocked K cache: K_fb[row / 16][kvh]
-//      [feature][row % 16], so the 16 keys of one feature are one 32-byte sector
-//      and a feature no draw kept costs no DRAM traffic.  One warp per 32-key
-//      chunk, lane = key: x_g = scale * sum over the list of c_g,j k_j, then the
-//      chunk's record (m, z) and exp(x - m) into the stash, exactly the outputs of
-//      the token-major pass 1.
+//   2. fb_pass1_kernel, pass 1 on a feature-blocked K cache: K_fb[row / 64][kvh]
+//      [feature][row % 64], so the 64 keys of one feature are one 128-byte line
+//      (bf16) and a feature no draw kept costs no DRAM traffic.  (With 16 keys per
+//      32-byte sector the saving vanished: GB300's DRAM traffic, measured, comes
+//      in lines, and a line of 4 features almost always holds a kept one.)  One
+//      warp per 64 keys, two chunks: x_g = scale * sum over the list of c_g,j k_j,
+//      then each chunk's record (m, z) and exp(x - m) into the stash, exactly the
+//      outputs of the token-major pass 1.
 //   3. the cluster pass 2 of santa_decode_prop, unchanged.
 #include "santa_launch.h"
 #include "santa_stream.cuh"
@@ -111,15 +113,19 @@ __global__ void __launch_bounds__(128) bernoulli_query_kernel(const Params p) {
     }
 }
 
-// Pass 1 on the feature-blocked cache: warps walk (sequence, chunk, KV head) units
-// with a stride of the grid's warp count; a warp stages its group's list and
-// effective queries in shared memory when its (sequence, KV head) changes.
+// Pass 1 on the feature-blocked cache: warps walk (sequence, chunk pair, KV head)
+// units with a stride of the grid's warp count; a warp stages its group's list and
+// effective queries in shared memory when its (sequence, KV head) changes.  A unit
+// is 64 keys, chunks 2cp and 2cp + 1: lane l holds keys 64cp + l and 64cp + 32 + l,
+// so that for one feature the warp's two loads cover the feature's 128-byte line
+// of 64 keys (for bf16; a key block that starts mid-line touches two lines).
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kFbWarps * 32, 3) fb_pass1_kernel(const Params p) {
     __shared__ int s_list[kFbWarps][D];
     __shared__ float s_c[kFbWarps][G][D];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long units = (long long)p.B * p.nch * p.Hkv;
+    const int npair = (p.nch + 1) / 2;
+    const long long units = (long long)p.B * npair * p.Hkv;
     const long long stride = (long long)gridDim.x * kFbWarps;
     int cur_b = -1, cur_kvh = -1, nsel = 0, L = 0;
     long long start = 0;
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 3) fb_pass1_kernel(const Params
     for (long long u = (long long)blockIdx.x * kFbWarps + warp; u < units; u += stride) {
         const int kvh = int(u % p.Hkv);
         const long long r = u / p.Hkv;
-        const int b = int(r / p.nch), ch = int(r % p.nch);
+        const int b = int(r / npair), cp = int(r % npair);
         if (b != cur_b || kvh != cur_kvh) {
             __syncwarp();
             if (b != cur_b) L = seq_bounds(p, b, &start);
@@ -145,77 +151,89 @@ __global__ void __launch_bounds__(kFbWarps * 32, 3) fb_pass1_kernel(const Params
             }
             __syncwarp();
         }
-        if (ch * kChunkRows >= L) continue;  // past the sequence: no record
-        const int key = ch * kChunkRows + lane;
-        const bool valid = key < L;
-        const long long row = start + (valid ? key : 0);
-        const T *kb = kfb + ((size_t(row >> 4) * p.Hkv + kvh) * D) * 16 + (row & 15);
-        float x[G];
+        const int key0 = cp * 2 * kChunkRows;
+        if (key0 >= L) continue;  // past the sequence: no record
+        const int ka = key0 + lane, kb = ka + kChunkRows;
+        const bool va = ka < L, vb = kb < L;
+        const long long ra = start + (va ? ka : key0), rb = start + (vb ? kb : key0);
+        const T *pa = kfb + ((size_t(ra >> 6) * p.Hkv + kvh) * D) * 64 + (ra & 63);
+        const T *pb = kfb + ((size_t(rb >> 6) * p.Hkv + kvh) * D) * 64 + (rb & 63);
+        float xa[G], xb[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) x[g] = 0.f;
-        // kFbBatch features at a time: that many independent loads of the warp in flight
+        for (int g = 0; g < G; ++g) xa[g] = xb[g] = 0.f;
+        // kFbBatch / 2 features at a time: kFbBatch independent loads of the warp in flight
+        constexpr int kF = kFbBatch / 2;
         int j = 0;
-        for (; j + kFbBatch <= nsel; j += kFbBatch) {
-            T kr[kFbBatch];
+        for (; j + kF <= nsel; j += kF) {
+            T ea[kF], eb[kF];
 #pragma unroll
-            for (int t = 0; t < kFbBatch; ++t) kr[t] = __ldg(kb + s_list[warp][j + t] * 16);
-#pragma unroll
-            for (int t = 0; t < kFbBatch; ++t) {
-                const float kv = to_float<T>(kr[t]);
-#pragma unroll
-                for (int g = 0; g < G; ++g) x[g] = fmaf(s_c[warp][g][j + t], kv, x[g]);
+            for (int t = 0; t < kF; ++t) {
+                const int off = s_list[warp][j + t] * 64;
+                ea[t] = __ldg(pa + off);
+                eb[t] = __ldg(pb + off);
             }
-        }
-        for (; j + 8 <= nsel; j += 8) {
-            T kr[8];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) kr[t] = __ldg(kb + s_list[warp][j + t] * 16);
+            for (int t = 0; t < kF; ++t) {
+                const float fa = to_float<T>(ea[t]), fb = to_float<T>(eb[t]);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const float kv = to_float<T>(kr[t]);
-#pragma unroll
-                for (int g = 0; g < G; ++g) x[g] = fmaf(s_c[warp][g][j + t], kv, x[g]);
+                for (int g = 0; g < G; ++g) {
+                    const float c = s_c[warp][g][j + t];
+                    xa[g] = fmaf(c, fa, xa[g]);
+                    xb[g] = fmaf(c, fb, xb[g]);
+                }
             }
         }
         for (; j < nsel; ++j) {
-            const float kv = to_float<T>(__ldg(kb + s_list[warp][j] * 16));
+            const int off = s_list[warp][j] * 64;
+            const float fa = to_float<T>(__ldg(pa + off)), fb = to_float<T>(__ldg(pb + off));
 #pragma unroll
-            for (int g = 0; g < G; ++g) x[g] = fmaf(s_c[warp][g][j], kv, x[g]);
+            for (int g = 0; g < G; ++g) {
+                const float c = s_c[warp][g][j];
+                xa[g] = fmaf(c, fa, xa[g]);
+                xb[g] = fmaf(c, fb, xb[g]);
+            }
         }
+        // the two chunks' records and stash rows
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float xs = valid ? x[g] * p.scale : -INFINITY;
-            const float m = warp_max(xs);
-            const float e = valid ? __expf(xs - m) : 0.f;
-            const float z = warp_sum(e);
-            const size_t hq = size_t(b) * p.Hq + size_t(kvh) * G + g;
-            p.stash[(hq * p.nch + ch) * kChunkRows + lane] = e;
-            if (lane == 0) store_record(p.rec + hq * p.nch + ch, m, z);
+        for (int half = 0; half < 2; ++half) {
+            const int ch = 2 * cp + half;
+            if (ch * kChunkRows >= L) break;
+            const bool valid = half ? vb : va;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float xs = valid ? (half ? xb[g] : xa[g]) * p.scale : -INFINITY;
+                const float m = warp_max(xs);
+                const float e = valid ? __expf(xs - m) : 0.f;
+                const float z = warp_sum(e);
+                const size_t hq = size_t(b) * p.Hq + size_t(kvh) * G + g;
+                p.stash[(hq * p.nch + ch) * kChunkRows + lane] = e;
+                if (lane == 0) store_record(p.rec + hq * p.nch + ch, m, z);
+            }
         }
     }
 }
 
-// Token-major [rows][Hkv][D] to feature-blocked [ceil(rows / 16)][Hkv][D][16]
+// Token-major [rows][Hkv][D] to feature-blocked [ceil(rows / 64)][Hkv][D][64]
 // (rows past the end are zero).
 template <typename T>
 __global__ void feature_block_kernel(const T *k, T *kfb, long long rows, int hkv, int D) {
-    const long long blocks = (rows + 15) / 16;
-    const long long n = blocks * hkv * D * 16;
+    const long long blocks = (rows + 63) / 64;
+    const long long n = blocks * hkv * D * 64;
     for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < n; o += (long long)gridDim.x * blockDim.x) {
-        const int pos = int(o & 15);
-        const long long rest = o >> 4;
+        const int pos = int(o & 63);
+        const long long rest = o >> 6;
         const int f = int(rest % D);
         const long long bh = rest / D;
         const int h = int(bh % hkv);
         const long long blk = bh / hkv;
-        const long long row = blk * 16 + pos;
+        const long long row = blk * 64 + pos;
         kfb[o] = row < rows ? k[(row * hkv + h) * D + f] : T(0);
     }
 }
 
 cudaError_t launch_feature_block(int dtype, const void *k, void *kfb, long long rows, int hkv, int D,
                                  cudaStream_t stream) {
-    const long long n = (rows + 15) / 16 * hkv * D * 16;
+    const long long n = (rows + 63) / 64 * hkv * D * 64;
     const unsigned blocks = unsigned(n / 256 + 1 < 4096 ? n / 256 + 1 : 4096);
     if (dtype == SANTA_BF16)
         feature_block_kernel<uint16_t><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(k),
@@ -239,7 +257,7 @@ cudaError_t launch_prop_bernoulli(const Params &p, int dtype, cudaStream_t strea
         cudaError_t e1 = cudaGetLastError();
         if (e1 != cudaSuccess) return e1;
         // three CTAs of 8 warps per SM, each warp with up to kFbBatch loads in flight
-        const long long units = (long long)p.B * p.nch * p.Hkv;
+        const long long units = (long long)p.B * ((p.nch + 1) / 2) * p.Hkv;
         long long grid = (long long)sms * 3;
         if (grid > (units + kFbWarps - 1) / kFbWarps) grid = (units + kFbWarps - 1) / kFbWarps;
         if (grid < 1) grid = 1;

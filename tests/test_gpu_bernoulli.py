@@ -134,14 +134,14 @@ def test_all_probabilities_one_is_plain_prop():
 
 
 def test_feature_blocked_copy_is_exact():
-    """K_fb[r / 16][h][f][r % 16] = K[r][h][f]; rows past the end are zero."""
+    """K_fb[r / 64][h][f][r % 64] = K[r][h][f]; rows past the end are zero."""
     inp = generate(SMALL[0])
     dec = decoder_for(inp)
     _, k, _, _, _ = to_torch(inp)
     kfb = dec.feature_blocked(k)
     rows, hkv, d = k.shape
-    nb = -(-rows // 16)
-    pad = torch.zeros((nb * 16 - rows, hkv, d), dtype=k.dtype, device=k.device)
-    expect = torch.cat([k, pad]).view(nb, 16, hkv, d).permute(0, 2, 3, 1).contiguous().view(-1)
+    nb = -(-rows // 64)
+    pad = torch.zeros((nb * 64 - rows, hkv, d), dtype=k.dtype, device=k.device)
+    expect = torch.cat([k, pad]).view(nb, 64, hkv, d).permute(0, 2, 3, 1).contiguous().view(-1)
     assert torch.equal(kfb.view(torch.int16), expect.view(torch.int16)) if k.dtype == torch.bfloat16 else \
         torch.equal(kfb, expect)
