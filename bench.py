@@ -65,10 +65,11 @@ def parse_args(argv=None):
 
 
 # The launches of one --profile round that the profiler filter
-# regex:"prop_stream|prop_pass2|fb_pass1|exact_stream|merge_kernel|tile_kernel|prop_fused" matches:
+# regex:"prop_stream|prop_pass2|fb_pass1|exact_stream|merge_kernel|flash_sample|prop_fused" matches:
 # prop (stream, pass 2), Bernoulli with the mean group query (feature-blocked pass 1,
-# pass 2), exact (stream, merge), flash at S = 2048 (tiles, merge), the fused kernel.
-PROFILE_ROUND_LAUNCHES = 9
+# pass 2), exact (stream, merge), flash at S = 2048 (stream, tile sampler, merge),
+# the fused kernel.
+PROFILE_ROUND_LAUNCHES = 10
 
 
 def run_profile(args) -> dict:
@@ -258,9 +259,11 @@ def byte_model(inp, mode: str, S: int, sample_idx=None):
            read by pass 2: 2 * 8 * Hq * sum ceil(L / 32)) + the stash of the
            chunks that received samples (4 * len per chunk) + the distinct V
            rows the samples touch (d * e each, per KV head) + out.
-    flash: K + q + distinct V rows + tile partials and records (written and read) + out.
+    flash: prop's pass 1 (K + q + stash write + chunk records) + the whole stash and
+           the chunk records read back by the tiles' sampler + distinct V rows +
+           tile partials and records (written and read) + out.
     exact: K + V + q + out (its split-KV partials are overhead, not counted).
-    Pass 1 / the tile kernel: K + q + its writes.
+    Pass 1: K + q + its writes.
     """
     w = inp.workload
     e = 2 if w.dtype == "bf16" else 4
@@ -290,10 +293,11 @@ def byte_model(inp, mode: str, S: int, sample_idx=None):
         main = K + q + Hq * sumL * 4 + rec
         total = main + rec + stash_read + vrows * d * e + out
     elif mode == "flash":
+        crec = 8 * Hq * sumC  # (m_c, z_c) per (b, h, chunk)
         rec = 8 * Hq * sumT  # (m_t, z_t) per (b, h, t)
         part = 4 * Hq * sumT * d
-        main = K + q + rec + part + vrows * d * e
-        total = main + rec + part + out
+        main = K + q + Hq * sumL * 4 + crec
+        total = main + Hq * sumL * 4 + crec + vrows * d * e + 2 * (rec + part) + out
     else:
         # the dense method's own bytes; the split-KV partials of the streaming
         # kernel (one (M, Z, O) per warp and head) are overhead, not counted
@@ -477,7 +481,7 @@ def run_ours(args, dist: Dist):
                            "rotating K copies (median of 5 replays)"}
         del gm, dec1
     else:
-        kernel_name = {"flash": "flash_tile", "exact": "exact_stream"}[args.mode]
+        kernel_name = {"flash": "prop_pass1", "exact": "exact_stream"}[args.mode]
         main_us = main_us_eager
         main_bytes = bm["main"]
         main_timing = "CUDA events around the kernel inside each call, eager launches"

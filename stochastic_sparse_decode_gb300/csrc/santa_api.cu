@@ -68,7 +68,9 @@ int check_problem(const santa_problem *p, int mode) {
 //                bytes and their counts [B][Hkv]; the header, counters and records
 //                must be zero before the first call (`clear` bytes from the start) and
 //                every call leaves them so;
-//   flash:       tile records rec_m, rec_z [B][Hq][Tmax] and tile estimates [B][Hq][Tmax][d];
+//   flash:       the regions of prop up to the chunk offsets (its pass 1 is prop's
+//                streaming pass; nothing needs to start at zero), then the tile records
+//                rec_m, rec_z [B][Hq][Tmax] and the tile estimates [B][Hq][Tmax][d];
 //   exact:       per (sequence, streaming warp, head of the group) the partial state
 //                (M, Z) as rec_m [B][P][G][2] and O as [B][P][G][d], P the warps of
 //                the streaming kernel's largest grid.
@@ -93,30 +95,33 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
         return SANTA_OK;
     }
     const double nrec = B * Hq * (prop ? nch : Tmax);
-    double est = 2 * nrec * 4;
+    const double nchunk = B * Hq * nch;  // prop and flash both run the streaming pass 1
+    double est = nchunk * (8 + 32 * 4 + 1) + B * Hq * 8;
     if (prop)
-        est += nrec * 32 * 4 + B * Hq * (kPropMaxSplit * D * 4 + 4);
+        est += B * Hq * (kPropMaxSplit * D * 4 + D * 4) + B * p->num_kv_heads * (D + 4);
     else
-        est += nrec * D * 4;
+        est += nrec * (D + 2) * 4;
     if (est > 1e15) return SANTA_INVALID_ARG;
 
-    const size_t n_rec = size_t(p->batch) * p->num_q_heads * size_t(prop ? nch : Tmax);
+    const size_t n_chunk = size_t(p->batch) * p->num_q_heads * size_t(nch);
+    const size_t n_tile = size_t(p->batch) * p->num_q_heads * size_t(Tmax);
     size_t off = 0;
     L->Tmax = Tmax;
     L->nch = nch;
+    // the streaming pass 1's outputs (prop and flash)
+    off = 256;  // header
+    L->cnt = off;
+    off += align256(size_t(p->batch) * p->num_q_heads * 4);
+    L->rec = off;
+    off += align256(n_chunk * 8);
+    L->clear = prop ? off : 0;  // only prop's samplers need the bytes before here zero
+    L->done = off;
+    off += align256(size_t(p->batch) * p->num_q_heads * 4);
+    L->stash = off;
+    off += align256(n_chunk * 32 * 4);
+    L->amax = off;
+    off += align256(size_t(p->batch) * p->num_q_heads * size_t((nch + 3) & ~3));
     if (prop) {
-        off = 256;  // header
-        L->cnt = off;
-        off += align256(size_t(p->batch) * p->num_q_heads * 4);
-        L->rec = off;
-        off += align256(n_rec * 8);
-        L->clear = off;
-        L->done = off;
-        off += align256(size_t(p->batch) * p->num_q_heads * 4);
-        L->stash = off;
-        off += align256(n_rec * 32 * 4);
-        L->amax = off;
-        off += align256(size_t(p->batch) * p->num_q_heads * size_t((nch + 3) & ~3));
         L->part = off;
         const long long heads = (long long)p->batch * p->num_q_heads;
         off += align256(size_t(heads) * prop_split_bound(heads) * p->head_dim * 4);
@@ -127,13 +132,13 @@ int make_layout(const santa_problem *p, int mode, Layout *L) {
         off += align256(groups * p->head_dim);
         L->tq_cnt = off;
         off += align256(groups * 4);
-    } else {
+    } else {  // flash: per tile (m_t, z_t) and the tile estimates
         L->rec_m = off;
-        off += align256(n_rec * 4);
+        off += align256(n_tile * 4);
         L->rec_z = off;
-        off += align256(n_rec * 4);
+        off += align256(n_tile * 4);
         L->partial = off;
-        off += align256(n_rec * p->head_dim * 4);
+        off += align256(n_tile * p->head_dim * 4);
     }
     L->total = off > 256 ? off : 256;
     return SANTA_OK;
@@ -152,7 +157,8 @@ int smem_check(const santa_problem *p, int mode, int sampler, bool paged) {
         const size_t s2 = prop_pass2_smem(p->head_dim, cps, sampler, p->S, paged);
         if (s2 > need) need = s2;
     } else if (mode == SANTA_MODE_FLASH) {
-        need = flash_tile_smem(p->dtype, p->head_dim, G, p->tile);
+        need = prop_pass1_smem(p->dtype, p->head_dim, G, int(kOptin));
+        if (flash_sample_smem(p->tile) > need) need = flash_sample_smem(p->tile);
     } else {
         need = exact_stream_smem(p->dtype, p->head_dim, G);
     }
@@ -304,16 +310,18 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
     prm.u_samples = sampler == kSys ? nullptr : U;
     prm.sampler = sampler;
     prm.out = out;
-    if (mode == SANTA_MODE_PROP) {
+    if (mode == SANTA_MODE_PROP || mode == SANTA_MODE_FLASH) {  // the streaming pass 1's outputs
         prm.hdr = reinterpret_cast<unsigned int *>(ws);
         prm.rec = reinterpret_cast<unsigned long long *>(ws + L.rec);
         prm.cnt = reinterpret_cast<unsigned int *>(ws + L.cnt);
         prm.stash = reinterpret_cast<float *>(ws + L.stash);
         prm.amax = ws + L.amax;
         prm.done = reinterpret_cast<unsigned int *>(ws + L.done);
-        prm.part = reinterpret_cast<float *>(ws + L.part);
-        prm.nsplit = 1;  // set by the launcher
         prm.nch4 = (L.nch + 3) & ~3;
+        prm.nsplit = 1;  // set by the launcher
+    }
+    if (mode == SANTA_MODE_PROP) {
+        prm.part = reinterpret_cast<float *>(ws + L.part);
     } else {
         prm.rec_m = reinterpret_cast<float *>(ws + L.rec_m);
         prm.rec_z = reinterpret_cast<float *>(ws + L.rec_z);
@@ -348,7 +356,7 @@ int run(int mode, int sampler, const santa_problem *p, const void *q, const void
             return SANTA_CUDA_ERROR;
         e = launch_prop(prm, p->dtype, kmap, stream, tm, stages);
     } else if (mode == SANTA_MODE_FLASH) {
-        if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, kWarpRows))
+        if (!kv_map(&kmap, k, p->dtype, p->head_dim, p->num_kv_heads, p->total_tokens, 32))
             return SANTA_CUDA_ERROR;
         e = launch_flash(prm, p->dtype, kmap, stream, tm);
     } else {

@@ -15,8 +15,6 @@
 namespace santa {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kTileWarps = 4;    // warps of a tile CTA
-constexpr int kWarpRows = 64;    // K/V rows per TMA chunk of one tile-kernel warp (2 per lane)
 constexpr int kMergeThreads = 128;
 constexpr int kExactCtaBound = 160;  // exact: streaming CTAs at most (the workspace is sized for it)
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy

@@ -114,6 +114,7 @@ cudaError_t launch_prop_bernoulli(const Params &p, int dtype, cudaStream_t strea
 // Token-major K [rows][hkv][D] into the feature-blocked layout [ceil(rows/16)][hkv][D][16].
 cudaError_t launch_feature_block(int dtype, const void *k, void *kfb, long long rows, int hkv, int D,
                                  cudaStream_t stream);
+// kmap: the K descriptor with boxes of 32 rows (flash runs prop's streaming pass 1).
 cudaError_t launch_flash(const Params &p, int dtype, const CUtensorMap &kmap, cudaStream_t stream, const Timing &tm);
 cudaError_t launch_exact(const Params &p, int dtype, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          cudaStream_t stream, const Timing &tm);
@@ -126,7 +127,7 @@ size_t prop_pass1_smem(int dtype, int D, int G, int smem_optin);
 cudaError_t prop_pass2_split(int nch, int tile, long long heads, int *nsplit, int *cps);
 size_t prop_pass2_smem(int D, int cps, int sampler, int S, bool paged);
 size_t prop_fused_smem(int dtype, int D, int G, int sampler, int S, int smem_optin, int *nbuf);
-size_t flash_tile_smem(int dtype, int D, int G, int tile);
+size_t flash_sample_smem(int tile);
 size_t exact_stream_smem(int dtype, int D, int G);
 int exact_stream_warps(int dtype, int D, int G);
 

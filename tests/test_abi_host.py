@@ -96,8 +96,9 @@ def test_workspace_layout_matches_the_byte_model(sd):
     largest-key byte per chunk (rows rounded up to 4), the splits' d-float sums,
     min(8, 256 // (B Hq)) splits per head, and the Bernoulli score stage's effective
     queries [B][Hq][d] float, kept features [B][Hkv][d] bytes and their counts
-    [B][Hkv]; flash: 2 tile-record
-    arrays [B][Hq][T] and the tile estimates [B][Hq][T][d]; exact: the streaming
+    [B][Hkv]; flash: prop's regions up to the chunk offsets (its pass 1 is prop's
+    streaming pass), then 2 tile-record arrays [B][Hq][T] and the tile estimates
+    [B][Hq][T][d]; exact: the streaming
     warps' partial states; each rounded up to 256 B."""
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     p = _llama8b_problem(sd)
@@ -106,7 +107,9 @@ def test_workspace_layout_matches_the_byte_model(sd):
     prop = (256 + r(1 * 32 * 4) + r(1 * 32 * nch * 8) + r(1 * 32 * 4) + r(32 * nch * 32 * 4) + r(32 * nch)
             + r(32 * 8 * 128 * 4) + tq(1))
     assert sd.workspace_size(p, sd.MODE_PROP) == prop
-    flash = 2 * r(1 * 32 * T * 4) + r(1 * 32 * T * 128 * 4)
+    stream = lambda B, nch: (256 + r(B * 32 * 4) + r(B * 32 * nch * 8) + r(B * 32 * 4)  # noqa: E731
+                             + r(B * 32 * nch * 32 * 4) + r(B * 32 * ((nch + 3) // 4 * 4)))
+    flash = stream(1, nch) + 2 * r(1 * 32 * T * 4) + r(1 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_FLASH) == flash
     # exact: (M, Z) and O per (sequence, streaming warp, head of the group); the
     # streaming grid is at most 160 CTAs of 12 warps for bf16 at d = 128
@@ -115,7 +118,7 @@ def test_workspace_layout_matches_the_byte_model(sd):
     # ragged tail: T = ceil(max_len / tile), chunks = ceil(max_len / 32)
     p = _llama8b_problem(sd, batch=3, max_len=1000, total_tokens=2000, tile=128)
     T, nch = 8, 32
-    assert sd.workspace_size(p, sd.MODE_FLASH) == 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
+    assert sd.workspace_size(p, sd.MODE_FLASH) == stream(3, nch) + 2 * r(3 * 32 * T * 4) + r(3 * 32 * T * 128 * 4)
     assert sd.workspace_size(p, sd.MODE_PROP) == (256 + r(3 * 32 * 4) + r(3 * 32 * nch * 8) + r(3 * 32 * 4)
                                                   + r(3 * 32 * nch * 32 * 4) + r(3 * 32 * nch) + r(96 * 2 * 128 * 4)
                                                   + tq(3))
