@@ -15,7 +15,7 @@
 namespace santa {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
 constexpr int kExactCtaBound = 160;  // exact: streaming CTAs at most (the workspace is sized for it)
 constexpr long long kWaitCycles = 1LL << 31;  // ~1 s: bound on any wait for a copy
 constexpr int kPropMaxSplit = 8;  // prop: CTAs sharing one head's thresholds, at most

@@ -57,11 +57,17 @@ __device__ __forceinline__ float block_inclusive_scan(float v, float *scr, float
     return v + off;
 }
 
+// The merge of one (sequence, query head): its kMergeThreads / 32 warps take the
+// tiles t = warp, warp + warps, ... eight at a time (every load of a batch in flight
+// at once), lane = a D/32 slice of the estimates; then the warps' sums in warp order.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     constexpr int kNW = kMergeThreads / 32;
-    const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-    __shared__ float s_coef[kMergeThreads];
+    constexpr int kE = D / 32;
+    constexpr int kB = 8;  // tiles per batch of a warp
+    const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float red[kNW][D];
+    __shared__ float zs[kNW];
     __shared__ float scr[kNW];
 
     long long start;
@@ -77,23 +83,49 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     float mx = -INFINITY;
     for (int t = tid; t < Tb; t += kMergeThreads) mx = fmaxf(mx, __ldcg(p.rec_m + rec0 + t));
     const float M = block_max<kNW>(mx, scr);
-    float num = 0.f, zpart = 0.f;
-    for (int c0 = 0; c0 < Tb; c0 += kMergeThreads) {
-        const int t = c0 + tid;
-        float coef = 0.f;
-        if (t < Tb) {
-            coef = __ldcg(p.rec_z + rec0 + t) * expf(__ldcg(p.rec_m + rec0 + t) - M);
-            zpart += coef;
+
+    float acc[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) acc[e] = 0.f;
+    float zw = 0.f;  // the warp's sum of coefficients (the same in every lane)
+    for (int t0 = warp; t0 < Tb; t0 += kB * kNW) {
+        float m[kB], z[kB], o[kB][kE];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int t = t0 + u * kNW;
+            m[u] = -INFINITY;
+            z[u] = 0.f;
+#pragma unroll
+            for (int e = 0; e < kE; ++e) o[u][e] = 0.f;
+            if (t < Tb) {
+                m[u] = __ldcg(p.rec_m + rec0 + t);
+                z[u] = __ldcg(p.rec_z + rec0 + t);
+                const float *src = p.partial + (rec0 + t) * D + lane * kE;
+#pragma unroll
+                for (int e = 0; e < kE; ++e) o[u][e] = __ldcg(src + e);
+            }
         }
-        __syncthreads();
-        s_coef[tid] = coef;
-        __syncthreads();
-        const int n = min(kMergeThreads, Tb - c0);
-        if (tid < D)
-            for (int k = 0; k < n; ++k) num = fmaf(s_coef[k], __ldcg(p.partial + (rec0 + c0 + k) * D + tid), num);
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const float cf = z[u] > 0.f ? z[u] * expf(m[u] - M) : 0.f;
+            zw += cf;
+#pragma unroll
+            for (int e = 0; e < kE; ++e) acc[e] = fmaf(cf, o[u][e], acc[e]);
+        }
     }
-    const float Z = block_sum<kNW>(zpart, scr);
-    if (tid < D) outp[tid] = num / Z;
+#pragma unroll
+    for (int e = 0; e < kE; ++e) red[warp][lane * kE + e] = acc[e];
+    if (lane == 0) zs[warp] = zw;
+    __syncthreads();
+    if (tid < D) {
+        float num = 0.f, Z = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) {
+            num += red[w][tid];
+            Z += zs[w];
+        }
+        outp[tid] = num / Z;
+    }
 }
 
 }  // namespace santa
