@@ -24,8 +24,9 @@ constexpr int kFlashWarps = 4;  // tiles per CTA of the sampling kernel, one per
 size_t flash_sample_smem(int tile) { return size_t(kFlashWarps) * tile * 4; }
 
 // One warp per (sequence, query head, tile): the tile's record and estimate.
+// (eight CTAs per SM for bf16: the whole grid of the bench workload in one wave)
 template <typename T, int D>
-__global__ void __launch_bounds__(kFlashWarps * 32) flash_sample_kernel(const Params p) {
+__global__ void __launch_bounds__(kFlashWarps * 32, sizeof(T) == 2 ? 8 : 4) flash_sample_kernel(const Params p) {
     extern __shared__ __align__(16) float fs_smem[];  // [warp][tile] running sums
     constexpr int kE = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(kFlashWarps * 32) flash_sample_kernel(const Pa
             if (p.dbg_idx && s0 + lane < p.dbg_stride)
                 p.dbg_idx[(head * p.Tmax + t) * p.dbg_stride + s0 + lane] = j;
         }
-        gather_rows<T, D>(acc, vseq, vstride, j, n, lane);
+        gather_queue<T, D>(acc, vseq, vstride, j, n, lane);
     }
     float *o = p.partial + (head * p.Tmax + t) * D + lane * kE;
 #pragma unroll

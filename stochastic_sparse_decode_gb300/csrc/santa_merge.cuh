@@ -59,7 +59,10 @@ __device__ __forceinline__ float block_inclusive_scan(float v, float *scr, float
 
 // The merge of one (sequence, query head): its kMergeThreads / 32 warps take the
 // tiles t = warp, warp + warps, ... eight at a time (every load of a batch in flight
-// at once), lane = a D/32 slice of the estimates; then the warps' sums in warp order.
+// at once), lane = a D/32 slice of the estimates.  A warp keeps its sums on the scale
+// of the largest m_t it has seen (rescaling when a batch raises it), so no pass over
+// the records precedes the loads; the warps' sums are then brought to the common
+// maximum M and added in warp order: out = sum_t w_t o_t / sum_t w_t.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     constexpr int kNW = kMergeThreads / 32;
@@ -67,8 +70,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     constexpr int kB = 8;  // tiles per batch of a warp
     const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     __shared__ float red[kNW][D];
-    __shared__ float zs[kNW];
-    __shared__ float scr[kNW];
+    __shared__ float ms[kNW], zs[kNW];
 
     long long start;
     const int L = seq_bounds(p, b, &start);
@@ -80,14 +82,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     }
     const int Tb = (L + p.tile - 1) / p.tile;
     const size_t rec0 = (size_t(b) * p.Hq + hq) * p.Tmax;
-    float mx = -INFINITY;
-    for (int t = tid; t < Tb; t += kMergeThreads) mx = fmaxf(mx, __ldcg(p.rec_m + rec0 + t));
-    const float M = block_max<kNW>(mx, scr);
 
     float acc[kE];
 #pragma unroll
     for (int e = 0; e < kE; ++e) acc[e] = 0.f;
-    float zw = 0.f;  // the warp's sum of coefficients (the same in every lane)
+    float mw = -INFINITY, zw = 0.f;  // the warp's scale and sum of coefficients (the same in every lane)
     for (int t0 = warp; t0 < Tb; t0 += kB * kNW) {
         float m[kB], z[kB], o[kB][kE];
 #pragma unroll
@@ -105,9 +104,19 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
                 for (int e = 0; e < kE; ++e) o[u][e] = __ldcg(src + e);
             }
         }
+        float mb = mw;
+#pragma unroll
+        for (int u = 0; u < kB; ++u) mb = fmaxf(mb, m[u]);
+        if (mb > mw) {  // rescale what the warp holds to the batch's larger maximum
+            const float sc = mw > -INFINITY ? expf(mw - mb) : 0.f;
+            zw *= sc;
+#pragma unroll
+            for (int e = 0; e < kE; ++e) acc[e] *= sc;
+            mw = mb;
+        }
 #pragma unroll
         for (int u = 0; u < kB; ++u) {
-            const float cf = z[u] > 0.f ? z[u] * expf(m[u] - M) : 0.f;
+            const float cf = m[u] > -INFINITY ? z[u] * expf(m[u] - mw) : 0.f;
             zw += cf;
 #pragma unroll
             for (int e = 0; e < kE; ++e) acc[e] = fmaf(cf, o[u][e], acc[e]);
@@ -115,14 +124,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const Params p) {
     }
 #pragma unroll
     for (int e = 0; e < kE; ++e) red[warp][lane * kE + e] = acc[e];
-    if (lane == 0) zs[warp] = zw;
+    if (lane == 0) {
+        ms[warp] = mw;
+        zs[warp] = zw;
+    }
     __syncthreads();
     if (tid < D) {
+        float M = ms[0];
+#pragma unroll
+        for (int w = 1; w < kNW; ++w) M = fmaxf(M, ms[w]);
         float num = 0.f, Z = 0.f;
 #pragma unroll
         for (int w = 0; w < kNW; ++w) {
-            num += red[w][tid];
-            Z += zs[w];
+            const float sc = ms[w] > -INFINITY ? expf(ms[w] - M) : 0.f;
+            num = fmaf(red[w][tid], sc, num);
+            Z = fmaf(zs[w], sc, Z);
         }
         outp[tid] = num / Z;
     }

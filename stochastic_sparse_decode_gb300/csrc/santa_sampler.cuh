@@ -199,15 +199,15 @@ __device__ __forceinline__ void samp_bitonic_sort(float *a, int n, int tid) {
 
 // Adds V rows (one index per lane of `j`, the first n lanes) of one KV head to the
 // lane's slice accumulator (D/32 consecutive elements at lane D/32), rows added in
-// lane order.  The raw slices of up to 32 rows (16 for 16-byte slices) are in
-// flight at once, held undecoded.
+// lane order.  The raw slices of up to 16 rows are in flight at once, held
+// undecoded (32 rows for slices of up to 8 bytes measured no faster and spilled).
 template <typename T, int D>
 __device__ __forceinline__ void gather_queue(float (&acc)[D / 32], const T *vrow0, size_t row_stride, int j, int n,
                                              int lane) {
     constexpr int kE = D / 32;
     constexpr int kBytes = kE * int(sizeof(T));  // 4, 8 or 16
     constexpr int kWords = kBytes / 4;
-    constexpr int kFlight = kBytes <= 8 ? 16 : 16;
+    constexpr int kFlight = 16;
     for (int r0 = 0; r0 < n; r0 += kFlight) {
         uint32_t raw[kFlight][kWords];
 #pragma unroll
@@ -281,11 +281,11 @@ struct Thresholds {
 
 // ---- the sampler of one head
 //
-// Run by the kSampThreads threads of a CTA (tid = threadIdx.x, all warps, converged).
-// kWait: poll for chunks pass 1 has not finished yet (fused kernel); otherwise a
-// record that reads 0 counts as a chunk without mass and raises SANTA_ERR_WORKSPACE.
-// *give_up: set after a wait timed out (the grid's later heads are not waited for).
-template <typename T, int D, int SAMPLER, bool kPaged, bool kWait>
+// Run by the kSampThreads threads of a CTA (tid = threadIdx.x, all warps, converged),
+// after the CTA's own streaming: it polls for the chunks that pass 1 (other CTAs)
+// has not finished yet.  *give_up: set after a wait timed out (the grid's later
+// heads are not waited for).
+template <typename T, int D, int SAMPLER, bool kPaged>
 __device__ void sample_head(const Params &p, int b, int hq, int split, unsigned char *sm, int tid, bool *give_up) {
     using L = SampSmem<D>;
     using u64 = unsigned long long;
@@ -351,13 +351,11 @@ __device__ void sample_head(const Params &p, int b, int hq, int split, unsigned 
 
     // a workspace poisoned by an earlier timeout holds records nobody will reset
     bool stop = *give_up;
-    if constexpr (kWait) {
-        if (tid == 0) scri[2 * kSampWarps] = stop ? 0 : int(*reinterpret_cast<volatile unsigned int *>(p.hdr));
-        samp_sync();
-        if (scri[2 * kSampWarps] != 0) {
-            if (tid == 0) raise_flag(p, SANTA_ERR_WORKSPACE);
-            stop = true;
-        }
+    if (tid == 0) scri[2 * kSampWarps] = stop ? 0 : int(*reinterpret_cast<volatile unsigned int *>(p.hdr));
+    samp_sync();
+    if (scri[2 * kSampWarps] != 0) {
+        if (tid == 0) raise_flag(p, SANTA_ERR_WORKSPACE);
+        stop = true;
     }
     if (Nb == 0 || stop) {
         samp_sync();  // the scratch is reused by the next head
@@ -389,26 +387,23 @@ __device__ void sample_head(const Params &p, int b, int hq, int split, unsigned 
             missing += (c0 + i < Nb && r[i] == 0ull) ? 1 : 0;
         }
         unsigned pub = ld_relaxed_u32(cntp);
-        if constexpr (kWait) {
-            const long long t0 = clock64();
-            while (missing > 0 || pub < target) {
-                if (clock64() - t0 > limit) {
-                    timed_out = true;
-                    break;
-                }
-                __nanosleep(missing > 1 ? 128 : 32);
-                missing = 0;
-#pragma unroll
-                for (int i = 0; i < kSampReg; ++i)
-                    if (c0 + i < Nb && r[i] == 0ull) {
-                        r[i] = ld_relaxed_u64(recs + c0 + i);
-                        missing += r[i] == 0ull ? 1 : 0;
-                    }
-                pub = ld_relaxed_u32(cntp);
+        const long long t0 = clock64();
+        while (missing > 0 || pub < target) {
+            if (clock64() - t0 > limit) {
+                timed_out = true;
+                break;
             }
+            __nanosleep(missing > 1 ? 128 : 32);
+            missing = 0;
+#pragma unroll
+            for (int i = 0; i < kSampReg; ++i)
+                if (c0 + i < Nb && r[i] == 0ull) {
+                    r[i] = ld_relaxed_u64(recs + c0 + i);
+                    missing += r[i] == 0ull ? 1 : 0;
+                }
+            pub = ld_relaxed_u32(cntp);
         }
-        // (the sampler alone runs in stream order after pass 1: its counter is not needed)
-        empty_rec |= missing > 0 || (kWait && pub != unsigned(Nb));
+        empty_rec |= missing > 0 || pub != unsigned(Nb);
 #pragma unroll
         for (int i = 0; i < kSampReg; ++i)
             if (c0 + i < Nb && r[i] != 0ull) mx = fmaxf(mx, rec_m(r[i]));
@@ -416,7 +411,7 @@ __device__ void sample_head(const Params &p, int b, int hq, int split, unsigned 
     // Acquire side of the publication: the stash written before it is visible to
     // every load below (each thread fences after its own observation of the counter,
     // and the barrier below orders that before every thread's later loads).
-    if constexpr (kWait) __threadfence();
+    __threadfence();
     // the largest-logit offsets of this thread's chunks (one word: four bytes), for
     // the prefetch below
     const int ca0 = (nblk - 1) * kSampBlock + tid * kSampReg;
@@ -805,8 +800,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
             if (threadIdx.x < D) p.out[size_t(head) * D + threadIdx.x] = 0.f;
             continue;
         }
-        sample_head<T, D, SAMPLER, kPaged, true>(p, int(head / p.Hq), int(head % p.Hq), int(it % p.nsplit), smem,
-                                                 int(threadIdx.x), &give_up);
+        sample_head<T, D, SAMPLER, kPaged>(p, int(head / p.Hq), int(head % p.Hq), int(it % p.nsplit), smem,
+                                           int(threadIdx.x), &give_up);
     }
 }
 
