@@ -168,9 +168,10 @@ def measured_peaks():
 
 
 def source_digest() -> str:
-    """Digest of the device code (the kernels live in the .cuh headers)."""
+    """Digest of the device code (the kernels live in the .cuh headers and .cu files)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "stochastic_sparse_decode_gb300", "csrc", "*.cuh"))):
+    csrc = os.path.join(ROOT, "stochastic_sparse_decode_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cuh")) + glob.glob(os.path.join(csrc, "*.cu"))):
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
