@@ -273,3 +273,57 @@ def test_paged_problems_are_validated_before_any_launch(sd):
     assert call(nbytes=need - 1) == sd.WORKSPACE_TOO_SMALL
     assert L.santa_decode_prop_paged(ctypes.byref(p), None, dev, dev, dev, dev, dev, dev, need, None,
                                      None) == sd.INVALID_ARG
+
+
+def test_fused_prop_validates_like_prop(sd):
+    """santa_decode_prop_fused takes santa_decode_prop's arguments and checks them the same way."""
+    p = _llama8b_problem(sd)
+    t = _FakeTensor
+    ws = sd.workspace_size(p, sd.MODE_PROP)
+    for args, status in (((t(0x10000), t(0x20000), t(0x30000), t(0x40000), None, t(0x60000)), sd.INVALID_ARG),
+                         ((t(0x10000), t(0x20008), t(0x30000), t(0x40000), t(0x50000), t(0x60000)), sd.INVALID_ARG)):
+        with pytest.raises(sd.SantaError) as e:
+            sd.santa_decode_prop_fused(p, *args, t(0x100000, ws), stream=0)
+        assert e.value.status == status
+    with pytest.raises(sd.SantaError) as e:
+        sd.santa_decode_prop_fused(p, t(0x10000), t(0x20000), t(0x30000), t(0x40000), t(0x50000), t(0x60000),
+                                   t(0x100000, ws - 1), stream=0)
+    assert e.value.status == sd.WORKSPACE_TOO_SMALL
+
+
+def _call_bern(sd, p, u=0x70000, draws=4, group_mean=0, kfb=0x20000):
+    t = lambda a: None if a is None else _FakeTensor(a)  # noqa: E731
+    ws = sd.workspace_size(p, sd.MODE_PROP)
+    try:
+        sd.santa_decode_prop_bernoulli(p, t(0x10000), t(kfb), t(0x30000), t(0x40000), t(0x50000), t(u), draws,
+                                       group_mean, t(0x60000), _FakeTensor(0x100000, ws), stream=0)
+    except sd.SantaError as e:
+        return e.status
+    return sd.OK
+
+
+def test_bernoulli_arguments_are_checked(sd):
+    """1 <= draws <= 64, uniforms present and 4-byte aligned, K 16-byte aligned."""
+    p = _llama8b_problem(sd)
+    assert _call_bern(sd, p, draws=0) == sd.INVALID_ARG
+    assert _call_bern(sd, p, draws=65) == sd.INVALID_ARG
+    assert _call_bern(sd, p, u=None) == sd.INVALID_ARG
+    assert _call_bern(sd, p, u=0x70002) == sd.INVALID_ARG
+    assert _call_bern(sd, p, kfb=0x20008, group_mean=1) == sd.INVALID_ARG
+    # batch 0 is a no-op after the argument checks
+    assert _call_bern(sd, _llama8b_problem(sd, batch=0)) == sd.OK
+
+
+def test_feature_blocked_size_and_checks(sd):
+    """K_fb holds ceil(total_tokens / 64) blocks of Hkv x d x 64 elements; a buffer
+    too small or misaligned is refused before anything is enqueued."""
+    p = _llama8b_problem(sd, total_tokens=1000, max_len=1000)
+    n = sd.k_feature_blocked_size(p)
+    assert n == 16 * 8 * 128 * 64 * 2  # ceil(1000 / 64) = 16 blocks, bf16
+    t = _FakeTensor
+    with pytest.raises(sd.SantaError) as e:
+        sd.santa_k_feature_blocked(p, t(0x10000), t(0x200000, n - 1), stream=0)
+    assert e.value.status == sd.WORKSPACE_TOO_SMALL
+    with pytest.raises(sd.SantaError) as e:
+        sd.santa_k_feature_blocked(p, t(0x10008), t(0x200000, n), stream=0)
+    assert e.value.status == sd.INVALID_ARG
