@@ -179,7 +179,7 @@ int santa_workspace_init(const santa_problem *p, int mode, void *workspace, size
  * Workspace (santa_workspace_size bytes, 256-byte aligned regions): a 256-byte
  * header, per head a published-chunk counter, the chunk records
  * [B][Hq][ceil(max_len / 32)] as 64-bit words, per head a finished-split
- * counter (set by pass 1), the score stash [B][Hq][32 ceil(max_len / 32)]
+ * counter (the fused kernel's), the score stash [B][Hq][32 ceil(max_len / 32)]
  * float32, a byte per chunk and the fused kernel's per-split float32 sums;
  * zero-filled once before first use (see santa_workspace_init).  Supported up
  * to max_len = 2^22 keys (longer is SANTA_UNSUPPORTED).  Returns a status; see

@@ -787,7 +787,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
-    const bool failed = stream_chunks<T, D, G, kPaged>(kmap, p, nbuf, smem);
+    const bool failed = stream_chunks<T, D, G, kPaged, true>(kmap, p, nbuf, smem);
     if (failed && (threadIdx.x & 31) == 0) *s_failed = 1;
     __syncthreads();  // the CTA's stream is done: its chunk buffers are the samplers' now
     // a warp whose copy timed out may have left a copy in flight into the buffers:

@@ -233,7 +233,12 @@ __device__ __forceinline__ void publish_chunks(const Params &p, int b, int kvh, 
 // shared memory `smem` (1024-byte aligned) holds the streaming layout, after
 // stream_setup, a CTA barrier and the kernel's dependency wait.  Returns whether a
 // wait for one of the warp's copies timed out (after a bounded wait for the rest).
-template <typename T, int D, int G, bool kPaged>
+// kPublish (the fused kernel, whose samplers read the records while others are still
+// being written): publish the finished chunks, set the heads' finished-split
+// counters to 0 and store each chunk's largest-key offset.  Pass 1 alone does none
+// of the three: its reader starts after it ends, and a publication fence per
+// (sequence, KV head) a warp leaves measured ~25 us slower at batch 16.
+template <typename T, int D, int G, bool kPaged, bool kPublish>
 __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Params &p, int nbuf, unsigned char *smem) {
     using Geo = TileGeom<T, D>;
     using CG = ChunkGeom<T, D, G>;
@@ -296,7 +301,7 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
             int rec = len > 0 ? 1 : 0;
             // the group's finished-split counters start this call at 0 (published with
             // the chunk, before any split of the head can count itself in)
-            if (ch == 0)
+            if (kPublish && ch == 0)
                 for (int h = 0; h < G; ++h) p.done[size_t(b) * p.Hq + kvh * G + h] = 0u;
             long long row = lstart + ch * kChunkRows;
             if (kPaged && len > 0) {
@@ -347,6 +352,7 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
     // the next chunk in flight belongs to another (sequence, KV head), or none is.
     int pend = 0;
     auto finished = [&](const ChunkSlot &cs) {
+        if constexpr (!kPublish) return;  // pass 1 alone: its reader starts after it ends
         pend += cs.rec;
         __syncwarp();  // lane 0's slot descriptors of the chunks claimed since
         const bool last = n_done + 1 >= n_issued || slots[(n_done + 1) % nbuf].b != cs.b ||
@@ -436,7 +442,7 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
                     if (2 * t + j < G) {
                         const size_t hq = size_t(b) * p.Hq + kvh * G + 2 * t + j;
                         store_record(p.rec + hq * p.nch + ch, m[j], z[j]);
-                        p.amax[hq * p.nch4 + ch] = static_cast<unsigned char>(am[j]);
+                        if constexpr (kPublish) p.amax[hq * p.nch4 + ch] = static_cast<unsigned char>(am[j]);
                     }
             }
             finished(cs);
@@ -521,7 +527,7 @@ __device__ __forceinline__ bool stream_chunks(const CUtensorMap &kmap, const Par
             for (int o = kGH; o < 32; o <<= 1) am = min(am, __shfl_xor_sync(kFull, am, o));
             if (lane < kGH) {  // g8 = 0, l8 = lane: head `lane` of the pass
                 store_record(p.rec + (size_t(b) * p.Hq + hq) * p.nch + ch, m, z);
-                p.amax[(size_t(b) * p.Hq + hq) * p.nch4 + ch] = static_cast<unsigned char>(am);
+                if constexpr (kPublish) p.amax[(size_t(b) * p.Hq + hq) * p.nch4 + ch] = static_cast<unsigned char>(am);
             }
         }
         finished(cs);
@@ -560,7 +566,7 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1)
     // may produce q, K or read this call's workspace) must be complete below.
     pdl_wait();
     pdl_launch_dependents();
-    stream_chunks<T, D, G, kPaged>(kmap, p, nbuf, smem);
+    stream_chunks<T, D, G, kPaged, false>(kmap, p, nbuf, smem);
 }
 
 }  // namespace santa
