@@ -57,3 +57,31 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_profile_summaries_are_readable_by_the_bench():
+    """Every kernel summary under profiles/ gives the command that made it, the
+    digest of the kernel sources it was taken on and its DRAM bytes per launch, in
+    the form bench.py reads; the launch list exists."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    prof = os.path.join(ROOT, "profiles")
+    names = sorted(f for f in os.listdir(prof) if f.endswith(".md"))
+    assert "launches_prop_llama8b_32k_b1.md" in names
+    for f in names:
+        text = open(os.path.join(prof, f)).read()
+        assert "ncu " in text and "--clock-control none" in text, f
+        if f.startswith("launches_"):
+            continue
+        fields = {}
+        for line in text.splitlines():
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+        assert len(fields.get("source_digest", "")) == 16, f
+        assert float(fields["dram_bytes_per_launch"]) > 0, f
+    # the whole call's and pass 1's summaries are the ones the bench line uses
+    for kernel in ("prop_call", "prop_pass1"):
+        assert os.path.exists(os.path.join(prof, f"{kernel}_llama8b_32k_b1.md"))
+    assert len(bench.source_digest()) == 16
